@@ -1,0 +1,215 @@
+/*
+ * adahop.h -- C ABI of the GB300 (sm_103a) AdaHOP MXFP4 linear layer.
+ *
+ * Method: AdaHOP, "Fast and Accurate Low-Precision Training via Outlier-Pattern-Aware
+ * Rotation" (Kim, Khodamoradi, Denolf, Park; arXiv 2604.02525).  Each linear layer runs three
+ * GEMMs (Fig. 5): Fwd Y = X.W^T, dgrad dX = G_Y.W, wgrad dW = G_Y^T.X.  Every operand is
+ * classified once as Row-wise, Column-wise or None (abstract; Fig. 4: patterns are stable, so
+ * calibration is one-time), and each GEMM's operand pattern pair selects
+ *   IHT      -- block-32 Hadamard along the inner dimension on both operands, then MXFP4;
+ *   OE-Left  -- the top-r rows (by FOID score) of one operand go to a BF16 path, the residual
+ *               (those rows zeroed) gets IHT + MXFP4;
+ *   OE-Right -- the same with columns;
+ *   BF16     -- a plain BF16 GEMM;
+ *   MXFP4    -- plain MXFP4 without the Hadamard (the pages' "MXFP4" baseline, Table 3).
+ * The data path follows Fig. 9 and the appendix implementation notes: FOID -> IHT and
+ * quantisation -> fused MXFP4 + BF16 GEMM -> fused scatter-add.
+ *
+ * Conventions for every entry point
+ *   - All matrices are row-major.  bf16 tensors are passed as raw 16-bit patterns.
+ *     X is M x K, W is N x K, G_Y is M x N, Y is M x N, dX is M x K, dW is N x K.
+ *   - Pointers are DEVICE pointers unless stated; the caller owns every buffer.  The library
+ *     allocates no device memory: scratch lives in the caller's workspace.
+ *   - Every call is asynchronous on the given CUDA stream (NULL = legacy default stream)
+ *     unless documented as synchronous.  Host-side argument errors return before any launch.
+ *   - Shapes: M, N, K must be positive multiples of 128.  OE rank r: 0 <= r <= 256, a multiple
+ *     of 8, and r <= the number of lines it is drawn from.  Device pointers must be 16-byte
+ *     aligned and the workspace 256-byte aligned; otherwise ADAHOP_ERR_ALIGN.
+ *   - Inputs must be finite; results for NaN/Inf inputs are unspecified.
+ *   - A workspace must start with its first 256 bytes zeroed (the status word lives there).
+ *     A device-side failure (a bounded wait that ran out) is recorded in that status word;
+ *     adahop_get_device_status() reports and clears it.
+ */
+#ifndef ADAHOP_H
+#define ADAHOP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st *adahop_stream_t;
+
+typedef enum {
+  ADAHOP_OK = 0,
+  ADAHOP_ERR_INVALID_ARG = 1,   /* null pointer, bad enum value, bad option */
+  ADAHOP_ERR_SHAPE = 2,         /* dimension not a positive multiple of 128, bad rank */
+  ADAHOP_ERR_ALIGN = 3,         /* pointer misaligned */
+  ADAHOP_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (see adahop_last_cuda_error) */
+  ADAHOP_ERR_TIMEOUT = 5,       /* a device-side bounded wait gave up */
+  ADAHOP_ERR_UNSUPPORTED = 6,   /* device is not sm_103a / feature not built */
+  ADAHOP_ERR_WORKSPACE = 7      /* workspace missing or smaller than adahop_workspace_size() */
+} adahop_status;
+
+/* Outlier pattern of one tensor (abstract; Table 1). */
+typedef enum { ADAHOP_PAT_NONE = 0, ADAHOP_PAT_ROW = 1, ADAHOP_PAT_COL = 2 } adahop_pattern;
+
+/* Per-GEMM strategy (Fig. 5), plus the plain-MXFP4 baseline of Table 3. */
+typedef enum {
+  ADAHOP_IHT = 0, ADAHOP_OE_LEFT = 1, ADAHOP_OE_RIGHT = 2, ADAHOP_BF16 = 3, ADAHOP_MXFP4 = 4
+} adahop_strategy;
+
+typedef enum { ADAHOP_OUT_BF16 = 0, ADAHOP_OUT_FP32 = 1 } adahop_out_dtype;
+
+/* Calibration options.  tau: threshold on max/lower-median of the per-line mean squares
+ * (default 8.0); probe_len must be 64 (FOID probe, appendix FOID paragraph); oe_rank r
+ * (default 64, Fig. 10: rank 64 is the favourable trade-off). */
+typedef struct {
+  double tau;
+  int probe_len;
+  int oe_rank;
+} adahop_options;
+
+/* The calibration record.  x, w, gy: adahop_pattern.  fwd, dgrad, wgrad: adahop_strategy.
+ * rho: the ratios behind the decision (row, col) for X, W, G_Y.  A caller may override any
+ * field before passing the plan to the linear calls. */
+typedef struct {
+  int32_t x, w, gy;
+  int32_t fwd, dgrad, wgrad;
+  int32_t oe_rank;
+  int32_t reserved;
+  double rho[6];
+} adahop_plan;
+
+/* Fills *opt with the defaults (tau 8.0, probe 64, rank 64). */
+void adahop_default_options(adahop_options *opt);
+
+/* Plain-text name of a status code (static storage). */
+const char *adahop_status_string(adahop_status st);
+
+/* The last CUDA error string seen by this thread's calls (static storage; "" if none). */
+const char *adahop_last_cuda_error(void);
+
+/* Workspace bytes needed by adahop_linear_fwd / adahop_linear_bwd / adahop_calibrate for this
+ * plan and shape (the maximum over the three GEMMs; the GEMMs of one bwd call reuse it in
+ * stream order).  *bytes receives the size. */
+adahop_status adahop_workspace_size(const adahop_plan *plan, int64_t M, int64_t N, int64_t K,
+                                    size_t *bytes);
+
+/* One-time pattern calibration (Fig. 4: patterns are stable, enabling one-time calibration).
+ * For each of X (M x K), W (N x K) and G_Y (M x N; may be NULL -> None) it computes the mean
+ * square of every row and column on the GPU, then on the host rho = max / lower-median per
+ * axis; pattern = None if both rho < tau, else Column-wise if rho_col >= rho_row, else
+ * Row-wise.  The strategy of each GEMM is looked up from its pattern pair:
+ *   CN, NN -> IHT; RC, RN -> OE-Left; NC -> OE-Right; CC, RR, NR, CR -> BF16.
+ * SYNCHRONOUS: waits for the stream (it copies the statistics to the host).
+ * opt may be NULL (defaults). */
+adahop_status adahop_calibrate(const void *X, const void *W, const void *GY, int64_t M,
+                               int64_t N, int64_t K, const adahop_options *opt,
+                               adahop_plan *plan_out, void *workspace, size_t ws_bytes,
+                               adahop_stream_t stream);
+
+/* Forward GEMM Y = X.W^T (M x N) with plan->fwd.  out_dtype selects bf16 or fp32 Y. */
+adahop_status adahop_linear_fwd(const adahop_plan *plan, const void *X, const void *W,
+                                int64_t M, int64_t N, int64_t K, void *Y, int out_dtype,
+                                void *workspace, size_t ws_bytes, adahop_stream_t stream);
+
+/* Backward GEMMs dX = G_Y.W (M x K) with plan->dgrad and dW = G_Y^T.X (N x K) with
+ * plan->wgrad.  Either output may be NULL to skip that GEMM. */
+adahop_status adahop_linear_bwd(const adahop_plan *plan, const void *GY, const void *X,
+                                const void *W, int64_t M, int64_t N, int64_t K, void *dX,
+                                void *dW, int out_dtype, void *workspace, size_t ws_bytes,
+                                adahop_stream_t stream);
+
+/* Waits for the stream, then reads (and clears) the workspace status word.
+ * Returns ADAHOP_ERR_TIMEOUT if any kernel that used this workspace gave up a bounded wait. */
+adahop_status adahop_get_device_status(void *workspace, adahop_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Stage entry points (each is one step of Fig. 9; the linear calls above chain them).
+ * --------------------------------------------------------------------------------------- */
+
+/* FOID, Fast Outlier Index Detection (Fig. 9 caption; appendix FOID paragraph).
+ * T: rows x cols bf16.  axis 0: the lines are rows and the probe of row i is T[i, 0:64];
+ * axis 1: the lines are columns and the probe of column j is T[0:64, j].
+ * Score = float32 population variance of the probe (fixed pairwise summation tree, no FMA);
+ * idx_out (device, int32[r]) receives the r best lines in ascending order, ties to the lower
+ * index.  line_mask_out (device, may be NULL) receives a bitmap of ceil(lines/32) uint32 words
+ * with the selected lines set.  Needs adahop_foid_workspace_size() bytes of workspace. */
+adahop_status adahop_foid(const void *T, int64_t rows, int64_t cols, int axis, int r,
+                          int32_t *idx_out, uint32_t *line_mask_out, void *workspace,
+                          size_t ws_bytes, adahop_stream_t stream);
+size_t adahop_foid_workspace_size(int64_t lines, int r);
+
+/* IHT + MXFP4 quantisation (appendix, IHT and Quantization: 1D FWHT with block size 32 on
+ * the residual, then MXFP4 with 1D scaling).
+ * T: rows x cols bf16.  inner_axis 1: quantise along the columns (output lines = rows,
+ * J = cols); inner_axis 0: along the rows (output lines = cols, J = rows; the transposed
+ * orientation used by the backward GEMMs).
+ * zero_rows_mask / zero_cols_mask (device bitmaps over T's rows / cols, may be NULL): entries
+ * in those rows/columns are set to +0 first (the OE residual, appendix FOID paragraph).
+ * hadamard: 1 = apply the orthonormal Sylvester H32 per 32-block (butterflies 1..16 in
+ * float32, then times the float32 nearest 1/sqrt(32)); 0 = plain MXFP4.
+ * Per 32-block: E8M0 byte = clamp(floor(log2 amax) - 2 + 127, 0, 254) (0 for an all-zero
+ * block); codes = nearest E2M1, ties to even, saturating; sign bit from the element.
+ * codes: lines x J/2 bytes, J-contiguous, even element in the low nibble.
+ * scales: scale_layout 0 = lines x J/32 bytes (canonical); 1 = the tensor-core layout (atoms
+ * of 128 lines x 4 blocks, 512 bytes each, atom (l/128, b/4) at ((l/128)*(J/128) + b/4)*512,
+ * byte (l%32)*16 + ((l%128)/32)*4 + b%4 inside). */
+adahop_status adahop_quantize_mxfp4(const void *T, int64_t rows, int64_t cols, int inner_axis,
+                                    int hadamard, const uint32_t *zero_rows_mask,
+                                    const uint32_t *zero_cols_mask, uint8_t *codes,
+                                    uint8_t *scales, int scale_layout, adahop_stream_t stream);
+
+/* Outlier slice gather for the BF16 path.  T: rows x cols bf16; idx: int32[r] (device).
+ * mode 0: out[i, :] = T[idx[i], :]          (r x cols)
+ * mode 1: out[p, i] = T[p, idx[i]]          (rows x r)
+ * mode 2: out[q, i] = T[idx[i], q]          (cols x r)
+ * mode 3: out[i, p] = T[p, idx[i]]          (r x rows) */
+adahop_status adahop_gather(const void *T, int64_t rows, int64_t cols, const int32_t *idx,
+                            int r, int mode, void *out, adahop_stream_t stream);
+
+/* Fused MXFP4 (+ BF16 inner outlier) GEMM (appendix, Fused MXFP4+BF16 GEMM).
+ * C (P x Q) = deq(A) . deq(B)^T + A_o . B_o^T, accumulated in float32 in tensor memory.
+ * A: P x J MXFP4 (codes P x J/2, scales in layout 1), B: Q x J likewise.
+ * A_o: P x r bf16 and B_o: Q x r bf16 (r-contiguous; both NULL or r = 0 for no outlier term;
+ * r a multiple of 8).  C: bf16 or fp32 per out_dtype.  P, Q, J multiples of 128.
+ * The workspace only carries the status word (>= 256 bytes). */
+adahop_status adahop_gemm_mxfp4(const uint8_t *a_codes, const uint8_t *a_scales,
+                                const uint8_t *b_codes, const uint8_t *b_scales, int64_t P,
+                                int64_t Q, int64_t J, const void *A_o, const void *B_o, int r,
+                                void *C, int out_dtype, void *workspace, size_t ws_bytes,
+                                adahop_stream_t stream);
+
+/* BF16 GEMM C (P x Q) = A . B, float32 accumulation (Fig. 5's BF16 path; also the outlier
+ * GEMM of outer OE).  a_kmajor 1: A stored P x J (J-contiguous); 0: stored J x P.
+ * b_kmajor 1: B stored Q x J (i.e. B^T row-major); 0: stored J x Q.
+ * splits > 1 (only with c_partial): J is cut into `splits` ranges and partial sums go to
+ * c_partial[s] (fp32, splits x P x Q) instead of C.  P >= 1 (a multiple of 64 when A is
+ * stored J x P); Q and J multiples of 64.  The workspace only carries the status word. */
+adahop_status adahop_gemm_bf16(const void *A, int a_kmajor, const void *B, int b_kmajor,
+                               int64_t P, int64_t Q, int64_t J, void *C, int out_dtype,
+                               int splits, float *c_partial, void *workspace, size_t ws_bytes,
+                               adahop_stream_t stream);
+
+/* Fused scatter-add (appendix, Fused Scatter-Add): adds the outlier product in place.
+ * partial: fp32, splits x r x Q (axis 0) or splits x P x r (axis 1), summed over splits.
+ * axis 0: C[idx[i], q] += sum_s partial[s, i, q];  axis 1: C[p, idx[i]] += sum_s partial[s, p, i].
+ * The sum is formed in float32 and rounded once to C's type. */
+adahop_status adahop_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype,
+                                 const float *partial, int splits, const int32_t *idx, int r,
+                                 int axis, adahop_stream_t stream);
+
+/* Calibration statistics: row_ms[i] = mean_j T[i,j]^2, col_ms[j] = mean_i T[i,j]^2 (float32,
+ * device).  Both outputs are overwritten. */
+adahop_status adahop_calibration_stats(const void *T, int64_t rows, int64_t cols, float *row_ms,
+                                       float *col_ms, adahop_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADAHOP_H */

@@ -1,0 +1,187 @@
+// K1: FOID, Fast Outlier Index Detection.
+//
+// AdaHOP, Fig. 9 caption and appendix FOID paragraph: the variance of the first 64 elements
+// along each row (or column) ranks the lines, and the top-k lines are the outliers.
+//
+// Score of line l (float32, one fixed order, no fused multiply-add):
+//   level 0: s[i] = x[i] + x[i+32], q[i] = x[i]^2 + x[i+32]^2            (i < 32)
+//   level k: s[i] += s[i + 2^(5-k)], q[i] += q[i + 2^(5-k)]               (k = 1..5)
+//   mean = s * (1/64); var = q * (1/64) - mean * mean; var <- +0 unless var > 0.
+// Ranking key = (float bits of var) << 32 | (0xFFFFFFFF - l): larger variance first, and for
+// equal variance the lower index first.  Keys are unique, so the top-r set is well defined.
+//
+// Stage 1 (grid): each CTA scores 2048 lines (512 threads x 4), sorts their keys in shared
+// memory (bitonic) and writes its best r.  Stage 2 (one CTA): sorts the candidates, keeps the
+// best r, writes their indices in ascending order and the bitmap of selected lines.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace adahop {
+
+namespace {
+
+constexpr int kFoidThreads = 512;
+constexpr int kFoidChunk = 2048;            // lines per stage-1 CTA
+constexpr int kFoidMergeMaxKeys = 8192;     // stage-2 shared-memory capacity (64 KB)
+
+__device__ __forceinline__ float bf(uint32_t b) { return __uint_as_float(b << 16); }
+
+// Level 0 of the tree for the pair (a = x[i], b = x[i+32]).
+__device__ __forceinline__ void level0(float a, float b, float &s, float &q) {
+  s = __fadd_rn(a, b);
+  q = __fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b));
+}
+
+template <int AXIS>
+__device__ __forceinline__ uint64_t foid_key(const uint16_t *__restrict__ T, int64_t cols,
+                                             int64_t line) {
+  float s[32], q[32];
+  if (AXIS == 0) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(T + line * cols);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {           // chunk k holds x[8k..8k+7], chunk k+4 x[8k+32..]
+      const uint4 lo = __ldg(p + k), hi = __ldg(p + k + 4);
+      const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w}, wh[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        level0(bf(wl[j] & 0xFFFFu), bf(wh[j] & 0xFFFFu), s[8 * k + 2 * j], q[8 * k + 2 * j]);
+        level0(bf(wl[j] >> 16), bf(wh[j] >> 16), s[8 * k + 2 * j + 1], q[8 * k + 2 * j + 1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float a = bf(__ldg(T + static_cast<int64_t>(i) * cols + line));
+      const float b = bf(__ldg(T + static_cast<int64_t>(i + 32) * cols + line));
+      level0(a, b, s[i], q[i]);
+    }
+  }
+#pragma unroll
+  for (int h = 16; h >= 1; h >>= 1) {
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      s[i] = __fadd_rn(s[i], s[i + h]);
+      q[i] = __fadd_rn(q[i], q[i + h]);
+    }
+  }
+  const float inv64 = 0.015625f;
+  const float mean = __fmul_rn(s[0], inv64);
+  float var = __fsub_rn(__fmul_rn(q[0], inv64), __fmul_rn(mean, mean));
+  if (!(var > 0.0f)) var = 0.0f;
+  return (static_cast<uint64_t>(__float_as_uint(var)) << 32) |
+         static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(line));
+}
+
+// In-place bitonic sort of n (power of two) keys in shared memory, descending.
+__device__ void bitonic_sort_desc(uint64_t *keys, int n) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint64_t a = keys[i], b = keys[ixj];
+          const bool up = (i & k) == 0;     // this run ends descending
+          if (up ? (a < b) : (a > b)) {
+            keys[i] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+template <int AXIS>
+__global__ void __launch_bounds__(kFoidThreads) foid_local_kernel(const uint16_t *__restrict__ T,
+                                                                  int64_t rows, int64_t cols, int r,
+                                                                  uint64_t *cand) {
+  __shared__ uint64_t keys[kFoidChunk];
+  const int64_t lines = AXIS == 0 ? rows : cols;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kFoidChunk;
+  for (int j = 0; j < kFoidChunk / kFoidThreads; ++j) {
+    const int local = threadIdx.x + j * kFoidThreads;
+    const int64_t line = base + local;
+    keys[local] = line < lines ? foid_key<AXIS>(T, cols, line) : 0ull;
+  }
+  __syncthreads();
+  bitonic_sort_desc(keys, kFoidChunk);
+  for (int i = threadIdx.x; i < r; i += blockDim.x)
+    cand[static_cast<int64_t>(blockIdx.x) * r + i] = keys[i];
+}
+
+__global__ void __launch_bounds__(1024) foid_merge_kernel(const uint64_t *cand, int ncand, int np2,
+                                                          int r, int64_t lines, int32_t *idx_out,
+                                                          uint32_t *mask_out) {
+  extern __shared__ uint64_t skeys[];
+  __shared__ uint32_t sidx[256];
+  for (int i = threadIdx.x; i < np2; i += blockDim.x) skeys[i] = i < ncand ? cand[i] : 0ull;
+  const int64_t words = (lines + 31) >> 5;
+  if (mask_out) {
+    for (int64_t w = threadIdx.x; w < words; w += blockDim.x) mask_out[w] = 0u;
+  }
+  __syncthreads();
+  if (r > 0) {
+    bitonic_sort_desc(skeys, np2);
+    // the best r lines, then ascending order (r <= 256; pad with 0xFFFFFFFF)
+    int rp2 = 1;
+    while (rp2 < r) rp2 <<= 1;
+    for (int i = threadIdx.x; i < rp2; i += blockDim.x)
+      sidx[i] = i < r ? 0xFFFFFFFFu - static_cast<uint32_t>(skeys[i] & 0xFFFFFFFFull) : 0xFFFFFFFFu;
+    __syncthreads();
+    for (int k = 2; k <= rp2; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = threadIdx.x; i < rp2; i += blockDim.x) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const uint32_t a = sidx[i], b = sidx[ixj];
+            const bool up = (i & k) == 0;   // ascending run
+            if (up ? (a > b) : (a < b)) {
+              sidx[i] = b;
+              sidx[ixj] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = threadIdx.x; i < r; i += blockDim.x) {
+      const uint32_t l = sidx[i];
+      idx_out[i] = static_cast<int32_t>(l);
+      if (mask_out) atomicOr(mask_out + (l >> 5), 1u << (l & 31));
+    }
+  }
+}
+
+}  // namespace
+
+size_t foid_scratch_bytes(int64_t lines, int r) {
+  const int64_t chunks = (lines + kFoidChunk - 1) / kFoidChunk;
+  return static_cast<size_t>(chunks * (r > 0 ? r : 1)) * sizeof(uint64_t);
+}
+
+cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
+                        int32_t *idx_out, uint32_t *mask_out, void *scratch, cudaStream_t s) {
+  const int64_t lines = axis == 0 ? rows : cols;
+  const int64_t chunks = (lines + kFoidChunk - 1) / kFoidChunk;
+  const int64_t ncand = chunks * r;
+  if (ncand > kFoidMergeMaxKeys || r > 256) return cudaErrorInvalidValue;
+  uint64_t *cand = static_cast<uint64_t *>(scratch);
+  if (r > 0) {
+    if (axis == 0)
+      foid_local_kernel<0><<<static_cast<unsigned>(chunks), kFoidThreads, 0, s>>>(T, rows, cols, r, cand);
+    else
+      foid_local_kernel<1><<<static_cast<unsigned>(chunks), kFoidThreads, 0, s>>>(T, rows, cols, r, cand);
+  }
+  int np2 = 1;
+  while (np2 < ncand) np2 <<= 1;
+  const size_t smem = static_cast<size_t>(np2) * sizeof(uint64_t);
+  cudaError_t e = cudaFuncSetAttribute(foid_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kFoidMergeMaxKeys * static_cast<int>(sizeof(uint64_t)));
+  if (e != cudaSuccess) return e;
+  foid_merge_kernel<<<1, 1024, smem, s>>>(cand, static_cast<int>(ncand), np2, r, lines, idx_out,
+                                          mask_out);
+  return cudaGetLastError();
+}
+
+}  // namespace adahop

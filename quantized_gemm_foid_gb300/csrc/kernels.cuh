@@ -1,0 +1,63 @@
+// Launch interfaces of the sm_103a kernels (host dispatcher <-> kernel translation units).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace adahop {
+
+// Byte offset of scale factor (line, 32-block blk) in the tensor-core scale layout: atoms of
+// 128 lines x 4 blocks (512 bytes), atom (line/128, blk/4) at ((line/128)*(J/128) + blk/4)*512,
+// and inside the atom byte (line%32)*16 + ((line%128)/32)*4 + blk%4.
+__host__ __device__ __forceinline__ int64_t tiled_sf_offset(int64_t line, int64_t blk, int64_t J) {
+  return ((line >> 7) * (J >> 7) + (blk >> 2)) * 512 + (line & 31) * 16 + ((line >> 5) & 3) * 4 +
+         (blk & 3);
+}
+
+struct QuantArgs {
+  const uint16_t *T;            // rows x cols bf16
+  int64_t rows, cols;
+  const uint32_t *zero_rows;    // bitmap over rows (may be null)
+  const uint32_t *zero_cols;    // bitmap over cols (may be null)
+  uint8_t *codes;
+  uint8_t *scales;
+  int hadamard;
+  int scale_layout;             // 0 canonical, 1 tensor-core atoms
+};
+cudaError_t launch_quant(const QuantArgs &a, int inner_axis, int num_sms, cudaStream_t s);
+
+// FOID: stage 1 (per 2048-line chunk top-r) + stage 2 (merge, ascending indices, bitmap).
+size_t foid_scratch_bytes(int64_t lines, int r);
+cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
+                        int32_t *idx_out, uint32_t *mask_out, void *scratch, cudaStream_t s);
+
+cudaError_t launch_gather(const uint16_t *T, int64_t rows, int64_t cols, const int32_t *idx, int r,
+                          int mode, uint16_t *out, cudaStream_t s);
+
+cudaError_t launch_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype, const float *partial,
+                               int splits, const int32_t *idx, int r, int axis, cudaStream_t s);
+
+cudaError_t launch_calib_stats(const uint16_t *T, int64_t rows, int64_t cols, float *row_ms,
+                               float *col_ms, cudaStream_t s);
+
+// tcgen05 GEMM (K3 MXFP4 + inner BF16 tail, K5/K6 BF16).
+struct GemmArgs {
+  int64_t P, Q, J;            // C is P x Q; inner dimension J
+  int kind;                   // 0 = MXFP4 (+ optional BF16 tail), 1 = BF16
+  int a_mn_major, b_mn_major; // BF16 only: operand stored J-major (MN contiguous)
+  const uint8_t *sfa, *sfb;   // MXFP4 scale factors (tensor-core layout)
+  int tail_stages;            // MXFP4: ceil(r / 64) stages of BF16 outlier MMAs
+  void *C;
+  int out_dtype;              // 0 bf16, 1 fp32
+  int splits;                 // BF16: split-K count (partials go to c_partial)
+  float *c_partial;
+  uint32_t *status;
+};
+struct GemmMaps {
+  CUtensorMap a, b, ao, bo;
+};
+cudaError_t launch_gemm(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s);
+size_t gemm_smem_bytes(int kind);
+
+}  // namespace adahop

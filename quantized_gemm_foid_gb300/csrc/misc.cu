@@ -1,0 +1,215 @@
+// K4 (fused scatter-add), the outlier-slice gathers of the BF16 path, and K7 (calibration
+// statistics).
+//
+// AdaHOP appendix implementation notes, "Fused Scatter-Add": the outlier product is added in
+// place into the residual GEMM's result.  Here the (possibly split-K) float32 partials are
+// summed in float32, added to C's current value in float32, and rounded once to C's type.
+// Calibration (one-time; Fig. 4 shows the patterns are stable): per-row and per-column mean
+// squares in float32, from one pass over the tensor.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace adahop {
+
+namespace {
+
+// ------------------------------------------------------------------------------- gathers
+// mode 0: out[i, :] = T[idx[i], :]   (r x cols), 16-byte copies
+__global__ void gather_rows_kernel(const uint16_t *__restrict__ T, int64_t cols,
+                                   const int32_t *__restrict__ idx, int r, uint16_t *out) {
+  const int64_t vec = cols >> 3;
+  const int64_t total = static_cast<int64_t>(r) * vec;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = t / vec, v = t - i * vec;
+    reinterpret_cast<uint4 *>(out + i * cols)[v] =
+        __ldg(reinterpret_cast<const uint4 *>(T + static_cast<int64_t>(idx[i]) * cols) + v);
+  }
+}
+// mode 1: out[p, i] = T[p, idx[i]]   (rows x r)
+__global__ void gather_cols_kernel(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
+                                   const int32_t *__restrict__ idx, int r, uint16_t *out) {
+  const int64_t total = rows * r;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t p = t / r, i = t - p * r;
+    out[t] = __ldg(T + p * cols + idx[i]);
+  }
+}
+// mode 2: out[q, i] = T[idx[i], q]   (cols x r): a 32-column x r tile through shared memory
+__global__ void gather_rows_t_kernel(const uint16_t *__restrict__ T, int64_t cols,
+                                     const int32_t *__restrict__ idx, int r, uint16_t *out) {
+  __shared__ uint16_t tile[256][34];
+  const int64_t q0 = static_cast<int64_t>(blockIdx.x) * 32;
+  for (int t = threadIdx.x; t < r * 32; t += blockDim.x) {
+    const int i = t >> 5, q = t & 31;
+    tile[i][q] = __ldg(T + static_cast<int64_t>(idx[i]) * cols + q0 + q);
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < r * 32; t += blockDim.x) {
+    const int q = t / r, i = t - q * r;
+    out[(q0 + q) * r + i] = tile[i][q];
+  }
+}
+// mode 3: out[i, p] = T[p, idx[i]]   (r x rows)
+__global__ void gather_cols_t_kernel(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
+                                     const int32_t *__restrict__ idx, int r, uint16_t *out) {
+  const int64_t total = rows * r;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = t / rows, p = t - i * rows;
+    out[t] = __ldg(T + p * cols + idx[i]);
+  }
+}
+
+// ------------------------------------------------------------------------------- scatter-add
+__device__ __forceinline__ float load_out(const float *p) { return *p; }
+__device__ __forceinline__ float load_out(const uint16_t *p) { return bf16_bits_to_f32(*p); }
+__device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(uint16_t *p, float v) {
+  *p = static_cast<uint16_t>(f32_to_bf16_bits(v));
+}
+
+// axis 0: C[idx[i], q] += sum_s partial[s, i, q]
+template <typename OutT>
+__global__ void scatter_rows_kernel(OutT *C, int64_t Q, const float *__restrict__ partial,
+                                    int splits, const int32_t *__restrict__ idx, int r) {
+  const int64_t total = static_cast<int64_t>(r) * Q;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = t / Q, q = t - i * Q;
+    float acc = 0.0f;
+    for (int s = 0; s < splits; ++s) acc += partial[s * total + t];
+    OutT *dst = C + static_cast<int64_t>(idx[i]) * Q + q;
+    store_out(dst, load_out(dst) + acc);
+  }
+}
+// axis 1: C[p, idx[i]] += sum_s partial[s, p, i]
+template <typename OutT>
+__global__ void scatter_cols_kernel(OutT *C, int64_t P, int64_t Q, const float *__restrict__ partial,
+                                    int splits, const int32_t *__restrict__ idx, int r) {
+  const int64_t total = P * r;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t p = t / r, i = t - p * r;
+    float acc = 0.0f;
+    for (int s = 0; s < splits; ++s) acc += partial[s * total + t];
+    OutT *dst = C + p * Q + idx[i];
+    store_out(dst, load_out(dst) + acc);
+  }
+}
+
+// ------------------------------------------------------------------------------- calibration
+// Block: 256 threads x 8 columns = 2048 columns; 64 rows per block.  Row sums are reduced per
+// block and added atomically; column sums are accumulated over the 64 rows and added atomically.
+constexpr int kCalRows = 64;
+__global__ void __launch_bounds__(256) calib_stats_kernel(const uint16_t *__restrict__ T,
+                                                          int64_t rows, int64_t cols,
+                                                          float *row_sum, float *col_sum) {
+  __shared__ float red[8];
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kCalRows;
+  const bool active = c0 < cols;
+  float colacc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int rr = 0; rr < kCalRows && r0 + rr < rows; ++rr) {
+    float rs = 0.0f;
+    if (active) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(T + (r0 + rr) * cols + c0));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float a = bf16_bits_to_f32(w[k] & 0xFFFFu), b = bf16_bits_to_f32(w[k] >> 16);
+        colacc[2 * k] += a * a;
+        colacc[2 * k + 1] += b * b;
+        rs += a * a + b * b;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xFFFFFFFFu, rs, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = rs;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.0f;
+      for (int k = 0; k < 8; ++k) t += red[k];
+      atomicAdd(row_sum + r0 + rr, t);
+    }
+    __syncthreads();
+  }
+  if (active) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) atomicAdd(col_sum + c0 + k, colacc[k]);
+  }
+}
+__global__ void scale_kernel(float *v, int64_t n, float s) {
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    v[t] *= s;
+}
+
+unsigned grid_for(int64_t work, int threads, int64_t cap = 8192) {
+  int64_t b = (work + threads - 1) / threads;
+  if (b < 1) b = 1;
+  if (b > cap) b = cap;
+  return static_cast<unsigned>(b);
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const uint16_t *T, int64_t rows, int64_t cols, const int32_t *idx, int r,
+                          int mode, uint16_t *out, cudaStream_t s) {
+  if (r == 0) return cudaSuccess;
+  switch (mode) {
+    case 0:
+      gather_rows_kernel<<<grid_for(r * (cols >> 3), 256), 256, 0, s>>>(T, cols, idx, r, out);
+      break;
+    case 1:
+      gather_cols_kernel<<<grid_for(rows * r, 256), 256, 0, s>>>(T, rows, cols, idx, r, out);
+      break;
+    case 2:
+      gather_rows_t_kernel<<<static_cast<unsigned>(cols / 32), 256, 0, s>>>(T, cols, idx, r, out);
+      break;
+    case 3:
+      gather_cols_t_kernel<<<grid_for(rows * r, 256), 256, 0, s>>>(T, rows, cols, idx, r, out);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype, const float *partial,
+                               int splits, const int32_t *idx, int r, int axis, cudaStream_t s) {
+  if (r == 0) return cudaSuccess;
+  const int64_t work = axis == 0 ? r * Q : P * r;
+  const unsigned g = grid_for(work, 256);
+  if (axis == 0) {
+    if (out_dtype == 1)
+      scatter_rows_kernel<float><<<g, 256, 0, s>>>(static_cast<float *>(C), Q, partial, splits, idx, r);
+    else
+      scatter_rows_kernel<uint16_t><<<g, 256, 0, s>>>(static_cast<uint16_t *>(C), Q, partial, splits,
+                                                      idx, r);
+  } else {
+    if (out_dtype == 1)
+      scatter_cols_kernel<float><<<g, 256, 0, s>>>(static_cast<float *>(C), P, Q, partial, splits,
+                                                   idx, r);
+    else
+      scatter_cols_kernel<uint16_t><<<g, 256, 0, s>>>(static_cast<uint16_t *>(C), P, Q, partial,
+                                                      splits, idx, r);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_calib_stats(const uint16_t *T, int64_t rows, int64_t cols, float *row_ms,
+                               float *col_ms, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(row_ms, 0, rows * sizeof(float), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(col_ms, 0, cols * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>((cols + 2047) / 2048),
+            static_cast<unsigned>((rows + kCalRows - 1) / kCalRows));
+  calib_stats_kernel<<<grid, 256, 0, s>>>(T, rows, cols, row_ms, col_ms);
+  scale_kernel<<<grid_for(rows, 256), 256, 0, s>>>(row_ms, rows, 1.0f / static_cast<float>(cols));
+  scale_kernel<<<grid_for(cols, 256), 256, 0, s>>>(col_ms, cols, 1.0f / static_cast<float>(rows));
+  return cudaGetLastError();
+}
+
+}  // namespace adahop

@@ -1,0 +1,91 @@
+"""Host-only checks of the C ABI: the library loads, exports every function declared in
+include/adahop.h, and rejects bad arguments before touching a device (no kernel launches)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "adahop.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(adahop_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_gemm_foid_gb300.build import build
+    build()
+    import quantized_gemm_foid_gb300 as q
+    return q
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    names = _declared_functions()
+    assert len(names) >= 15
+    raw = C.CDLL(lib.LIB._name)
+    for n in names:
+        assert hasattr(raw, n), n
+        assert n in lib.PROTOTYPES, f"{n} missing from the binding"
+    assert set(lib.PROTOTYPES) == set(names)
+
+
+def test_status_strings(lib):
+    for st in range(8):
+        assert lib.LIB.adahop_status_string(st)
+    assert lib.LIB.adahop_status_string(99) == b"unknown status"
+
+
+def test_default_options(lib):
+    o = lib.adahop_default_options()
+    assert (o.tau, o.probe_len, o.oe_rank) == (8.0, 64, 64)
+
+
+def test_workspace_size_validation(lib):
+    plan = lib.make_plan(oe_rank=64)
+    n = lib.adahop_workspace_size(plan, 4096, 2048, 8192)
+    assert n > 4096 * 8192 // 2
+    bad = C.c_size_t(0)
+    assert lib.LIB.adahop_workspace_size(C.byref(plan), 4096, 2048, 100, C.byref(bad)) == 2   # SHAPE
+    plan.fwd = 9
+    assert lib.LIB.adahop_workspace_size(C.byref(plan), 4096, 2048, 8192, C.byref(bad)) == 1  # INVALID
+    plan.fwd = 0
+    plan.oe_rank = 300
+    assert lib.LIB.adahop_workspace_size(C.byref(plan), 4096, 2048, 8192, C.byref(bad)) == 2
+    plan.oe_rank = 12        # not a multiple of 8
+    assert lib.LIB.adahop_workspace_size(C.byref(plan), 4096, 2048, 8192, C.byref(bad)) == 2
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    L = lib.LIB
+    plan = lib.make_plan()
+    # null tensors
+    assert L.adahop_linear_fwd(C.byref(plan), None, None, 128, 128, 128, None, 0, None, 0, None) == 1
+    # misaligned pointers are rejected before the device is queried
+    assert L.adahop_linear_fwd(C.byref(plan), 0x1001, 0x2000, 128, 128, 128, 0x3000, 0, 0x4000, 1 << 20, None) == 3
+    # bad output dtype
+    assert L.adahop_linear_fwd(C.byref(plan), 0x1000, 0x2000, 128, 128, 128, 0x3000, 7, 0x4000, 1 << 20, None) == 1
+    # bad shapes and a too-small workspace are caught before any device query
+    assert L.adahop_linear_fwd(C.byref(plan), 0x1000, 0x2000, 100, 128, 128, 0x3000, 0, 0x4000, 1 << 20, None) == 2
+    assert L.adahop_linear_fwd(C.byref(plan), 0x1000, 0x2000, 128, 128, 128, 0x3000, 0, 0x4000, 16, None) == 7
+    assert L.adahop_linear_bwd(C.byref(plan), 0x1000, 0x2000, 0x3000, 128, 128, 128, None, None, 0, 0x4000, 0,
+                               None) == 1
+    assert L.adahop_quantize_mxfp4(0x1000, 100, 128, 1, 1, None, None, 0x2000, 0x3000, 0, None) == 2
+    assert L.adahop_quantize_mxfp4(0x1000, 128, 128, 2, 1, None, None, 0x2000, 0x3000, 0, None) == 1
+    assert L.adahop_foid(0x1000, 128, 128, 0, 300, 0x2000, None, 0x3000, 1 << 20, None) == 2
+    assert L.adahop_gemm_bf16(0x1000, 1, 0x2000, 1, 128, 100, 128, 0x3000, 1, 1, None, 0x4000, 4096, None) == 2
+    assert L.adahop_gemm_mxfp4(0x1000, 0x1000, 0x1000, 0x1000, 128, 128, 128, None, None, 16, 0x2000, 1, 0x3000,
+                               4096, None) == 2
+    assert L.adahop_scatter_add(None, 1, 1, 0, None, 1, None, 0, 0, None) == 1
+    assert L.adahop_calibrate(None, None, None, 128, 128, 128, None, None, None, 0, None) == 1
+
+
+def test_python_binding_names_match_c(lib):
+    import quantized_gemm_foid_gb300.binding as b
+    for name in lib.PROTOTYPES:
+        if name in ("adahop_status_string", "adahop_last_cuda_error"):
+            continue
+        assert callable(getattr(b, name)), name

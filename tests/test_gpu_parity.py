@@ -1,0 +1,224 @@
+"""GPU <-> oracle parity through the C ABI (sm_103a library), on small and ragged shapes.
+
+Bar (from the method's statement of the target): bit-exact FOID indices, pattern classes, MXFP4
+codes and scales; GEMM outputs within relative Frobenius error 2e-3 of the oracle's float64
+product of the same dequantised operands for float32 output, 4e-3 for bf16 output (one extra
+bf16 rounding, 2^-9 relative per element).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synthetic import normal_bf16, bf16_bits
+from tests.gpu_util import (bitmap, dev_bf16_from_bits, from_tiled, to_dev, to_host_u8, to_tiled)
+
+pytestmark = pytest.mark.gpu
+
+TOL_FP32 = 2e-3
+TOL_BF16 = 4e-3
+
+
+@pytest.fixture(scope="module")
+def q():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_gemm_foid_gb300 as lib
+    return lib
+
+
+def _bits(shape, seed, std=1.0, axis=None, count=0, scale=1.0):
+    return bf16_bits(normal_bf16(*shape, std, seed, outlier_axis=axis, outlier_count=count,
+                                 outlier_scale=scale))
+
+
+# ------------------------------------------------------------------------------ K2 quantiser
+@pytest.mark.parametrize("shape", [(128, 128), (256, 512), (384, 1152)])
+@pytest.mark.parametrize("hadamard", [1, 0])
+@pytest.mark.parametrize("inner_axis", [1, 0])
+def test_quantize_bitexact(q, shape, hadamard, inner_axis):
+    T = _bits(shape, 11, axis="col", count=5, scale=50.0)
+    rows, cols = shape
+    zr = [0, 7, rows - 1]
+    zc = [3, 64, cols - 2]
+    ref_in = T if inner_axis == 1 else np.ascontiguousarray(T.T)
+    lines, J = ref_in.shape
+    dT = dev_bf16_from_bits(T)
+    for zero_rows, zero_cols in ((None, None), (zr, None), (None, zc), (zr, zc)):
+        codes = torch.zeros(lines * J // 2, dtype=torch.uint8, device="cuda")
+        scales = torch.zeros(lines * J // 32, dtype=torch.uint8, device="cuda")
+        mr = to_dev(bitmap(rows, zero_rows)) if zero_rows else None
+        mc = to_dev(bitmap(cols, zero_cols)) if zero_cols else None
+        q.adahop_quantize_mxfp4(dT, inner_axis, hadamard, mr, mc, codes, scales, 0)
+        torch.cuda.synchronize()
+        # the oracle's line/J view of the same zeroing
+        o_rows, o_cols = (zero_rows, zero_cols) if inner_axis == 1 else (zero_cols, zero_rows)
+        want_codes, want_scales = O.quantize_operand(ref_in, bool(hadamard), zero_rows=o_rows,
+                                                     zero_cols=o_cols)
+        got_codes = to_host_u8(codes).reshape(lines, J // 2)
+        got_scales = to_host_u8(scales).reshape(lines, J // 32)
+        assert np.array_equal(got_scales, want_scales)
+        assert np.array_equal(got_codes, want_codes)
+        # the tensor-core scale layout is the documented permutation of the canonical one
+        tiled = torch.zeros_like(scales)
+        q.adahop_quantize_mxfp4(dT, inner_axis, hadamard, mr, mc, codes, tiled, 1)
+        torch.cuda.synchronize()
+        assert np.array_equal(from_tiled(to_host_u8(tiled), lines, J), want_scales)
+
+
+def test_quantize_edge_values(q):
+    """All-zero blocks, tiny (subnormal-scale) blocks, exact ties and huge values."""
+    rows, cols = 128, 256
+    x = np.zeros((rows, cols), np.float32)
+    x[1, :32] = 2.0 ** -130 * np.arange(32)                    # subnormal amax
+    x[2, :32] = np.array([6, 5, 3.5, 2.5, 1.75, 1.25, 0.75, 0.25] * 4, np.float32)
+    x[3, :32] = -x[2, :32]
+    x[4, :] = 3.0e38 * np.cos(np.arange(cols))
+    x[5, :] = np.float32(1.5) ** (np.arange(cols) % 64 - 32)
+    T = O.f32_to_bf16_bits(x)
+    dT = dev_bf16_from_bits(T)
+    for had in (0, 1):
+        for inner in (1, 0):
+            ref_in = T if inner == 1 else np.ascontiguousarray(T.T)
+            lines, J = ref_in.shape
+            codes = torch.zeros(lines * J // 2, dtype=torch.uint8, device="cuda")
+            scales = torch.zeros(lines * J // 32, dtype=torch.uint8, device="cuda")
+            q.adahop_quantize_mxfp4(dT, inner, had, None, None, codes, scales, 0)
+            torch.cuda.synchronize()
+            wc, ws = O.quantize_operand(ref_in, bool(had))
+            assert np.array_equal(to_host_u8(scales).reshape(lines, -1), ws)
+            assert np.array_equal(to_host_u8(codes).reshape(lines, -1), wc)
+
+
+# ------------------------------------------------------------------------------ K1 FOID
+@pytest.mark.parametrize("axis", [0, 1])
+@pytest.mark.parametrize("shape,r", [((256, 512), 16), ((4096, 640), 64), ((128, 2560), 1),
+                                     ((640, 4224), 256), ((1024, 256), 0)])
+def test_foid_bitexact(q, axis, shape, r):
+    lines = shape[axis]
+    if r > lines:
+        pytest.skip("rank beyond lines")
+    T = _bits(shape, 21, axis="col" if axis else "row", count=min(8, r + 1), scale=40.0)
+    dT = dev_bf16_from_bits(T)
+    idx = torch.full((max(r, 1),), -1, dtype=torch.int32, device="cuda")
+    mask = torch.full(((lines + 31) // 32,), -1, dtype=torch.int32, device="cuda")
+    ws = q.new_workspace(q.adahop_foid_workspace_size(lines, r))
+    q.adahop_foid(dT, axis, r, idx, mask, ws)
+    torch.cuda.synchronize()
+    want = O.foid(T, "row" if axis == 0 else "col", r)
+    assert idx.cpu().numpy()[:r].tolist() == want.tolist()
+    assert np.array_equal(mask.cpu().numpy().view(np.uint32), bitmap(lines, want))
+
+
+def test_foid_ties_and_duplicates(q):
+    alt = np.where(np.arange(64) % 2, -1.0, 1.0)
+    x = np.tile(np.concatenate([alt, np.zeros(64)]), (300, 1)).astype(np.float32)
+    x[[5, 77, 150], :64] *= 3.0        # three clear winners, the rest tie
+    T = O.f32_to_bf16_bits(x)
+    dT = dev_bf16_from_bits(T)
+    for r in (3, 10, 64):
+        idx = torch.zeros(r, dtype=torch.int32, device="cuda")
+        ws = q.new_workspace(q.adahop_foid_workspace_size(300, r))
+        q.adahop_foid(dT, 0, r, idx, None, ws)
+        torch.cuda.synchronize()
+        assert idx.cpu().numpy().tolist() == O.foid(T, "row", r).tolist()
+
+
+# ------------------------------------------------------------------------------ calibration
+def test_calibration_classes(q):
+    from synthetic import WORKLOADS, tensor_recipes
+    wl = WORKLOADS["llama3.2-1b"]
+    for li in (0, 4):
+        X, W, GY = tensor_recipes(wl, li)
+        want = O.calibrate(bf16_bits(X), bf16_bits(W), bf16_bits(GY))
+        dX, dW, dG = X.cuda(), W.cuda(), GY.cuda()
+        M, K = X.shape
+        N = W.shape[0]
+        ws = q.new_workspace(4 * (max(M, N) + max(N, K)) + 4096)
+        plan = q.adahop_calibrate(dX, dW, dG, ws)
+        assert (plan.x, plan.w, plan.gy) == (want["patterns"]["X"], want["patterns"]["W"],
+                                             want["patterns"]["GY"])
+        assert (plan.fwd, plan.dgrad, plan.wgrad) == (want["fwd"], want["dgrad"], want["wgrad"])
+
+
+# ------------------------------------------------------------------------------ GEMMs
+def _rel(got, ref):
+    return O.rel_frobenius(got, ref)
+
+
+@pytest.mark.parametrize("P,Q,J", [(128, 256, 256), (256, 512, 384), (384, 384, 1024), (128, 128, 128)])
+@pytest.mark.parametrize("r", [0, 16, 64, 128])
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_gemm_mxfp4_against_oracle(q, P, Q, J, r, out):
+    A = _bits((P, J), 31, axis="col", count=4, scale=30.0)
+    Bt = _bits((Q, J), 32, std=0.02)
+    ac, asf = O.quantize_operand(A, True)
+    bc, bsf = O.quantize_operand(Bt, True)
+    ref = O.dequantize_operand(ac, asf) @ O.dequantize_operand(bc, bsf).T
+    Ao = Bo = None
+    if r:
+        Ao_bits = _bits((P, r), 33, std=5.0)
+        Bo_bits = _bits((Q, r), 34, std=0.02)
+        ref = ref + O.bf16_to_f32(Ao_bits).astype(np.float64) @ O.bf16_to_f32(Bo_bits).astype(np.float64).T
+        Ao, Bo = dev_bf16_from_bits(Ao_bits), dev_bf16_from_bits(Bo_bits)
+    C = torch.zeros((P, Q), dtype=torch.float32 if out == "fp32" else torch.bfloat16, device="cuda")
+    ws = q.new_workspace(4096)
+    q.adahop_gemm_mxfp4(to_dev(ac), to_dev(to_tiled(asf)), to_dev(bc), to_dev(to_tiled(bsf)), P, Q, J, Ao, Bo, r,
+                        C, ws)
+    assert q.adahop_get_device_status(ws) == 0
+    got = C.float().cpu().numpy().astype(np.float64)
+    assert _rel(got, ref) <= (TOL_FP32 if out == "fp32" else TOL_BF16)
+    if out == "fp32":
+        assert _rel(got, ref) <= 1e-5          # float32 accumulation of exact products
+
+
+@pytest.mark.parametrize("a_kmajor,b_kmajor", [(1, 1), (1, 0), (0, 0), (0, 1)])
+@pytest.mark.parametrize("P,Q,J", [(128, 256, 128), (256, 512, 320), (64, 192, 256)])
+def test_gemm_bf16_layouts(q, a_kmajor, b_kmajor, P, Q, J):
+    A = _bits((P, J), 41)              # logical A: P x J
+    B = _bits((J, Q), 42, std=0.5)     # logical B: J x Q
+    ref = O.bf16_to_f32(A).astype(np.float64) @ O.bf16_to_f32(B).astype(np.float64)
+    dA = dev_bf16_from_bits(A if a_kmajor else np.ascontiguousarray(A.T))
+    dB = dev_bf16_from_bits(np.ascontiguousarray(B.T) if b_kmajor else B)
+    C = torch.zeros((P, Q), dtype=torch.float32, device="cuda")
+    ws = q.new_workspace(4096)
+    q.adahop_gemm_bf16(dA, a_kmajor, dB, b_kmajor, P, Q, J, C, ws)
+    assert q.adahop_get_device_status(ws) == 0
+    assert _rel(C.cpu().numpy(), ref) <= 1e-5
+
+
+def test_gemm_bf16_split_partials(q):
+    P, Q, J, S = 64, 256, 1024, 4
+    A = _bits((P, J), 51)
+    B = _bits((J, Q), 52)
+    ref = O.bf16_to_f32(A).astype(np.float64) @ O.bf16_to_f32(B).astype(np.float64)
+    part = torch.zeros((S, P, Q), dtype=torch.float32, device="cuda")
+    ws = q.new_workspace(4096)
+    q.adahop_gemm_bf16(dev_bf16_from_bits(A), 1, dev_bf16_from_bits(B), 0, P, Q, J, None, ws, splits=S,
+                       c_partial=part)
+    torch.cuda.synchronize()
+    assert _rel(part.sum(0).cpu().numpy(), ref) <= 1e-5
+
+
+# ------------------------------------------------------------------------------ scatter-add
+@pytest.mark.parametrize("axis", [0, 1])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_scatter_add(q, axis, dtype):
+    P, Q, r, S = 256, 384, 24, 3
+    rng = np.random.default_rng(5)
+    idx = np.sort(rng.choice(P if axis == 0 else Q, r, replace=False)).astype(np.int32)
+    C0 = rng.standard_normal((P, Q)).astype(np.float32)
+    part = rng.standard_normal((S, r, Q) if axis == 0 else (S, P, r)).astype(np.float32)
+    dC = torch.from_numpy(C0).to(dtype).cuda()
+    base = dC.float().cpu().numpy().astype(np.float64)
+    q.adahop_scatter_add(dC, to_dev(part), S, to_dev(idx), r, axis)
+    torch.cuda.synchronize()
+    want = base.copy()
+    summed = part.astype(np.float32).sum(0, dtype=np.float32)
+    if axis == 0:
+        want[idx, :] = (base[idx, :].astype(np.float32) + summed).astype(np.float64)
+    else:
+        want[:, idx] = (base[:, idx].astype(np.float32) + summed).astype(np.float64)
+    got = dC.float().cpu().numpy()
+    tol = 1e-6 if dtype == torch.float32 else 2 ** -8
+    assert np.allclose(got, want, rtol=tol, atol=tol)
