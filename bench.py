@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""AdaHOP MXFP4 linear layer, forward + backward throughput on one GB300.
+
+Workload: the Llama3.1-8B-shaped block (tokens M = 4096 x 8 = 32768, hidden 4096, 8 KV heads x 128,
+FFN 14336): the q, k, v, o, gate, up and down linears, each running Fwd, dgrad and wgrad through
+the C ABI with the strategies chosen by one-time calibration (X Column-wise, W None, G_Y Row-wise
+-> Fwd CN: IHT, dgrad RN: OE-Left on G_Y rows (outer), wgrad RC: OE-Left on G_Y rows (inner)),
+OE rank 64, bf16 outputs.  One step = all seven linears' three GEMMs.  Inputs are seeded
+synthetic tensors (synthetic/), resident in HBM; every step touches ~15 GB, far above the 129 MB
+L2, so no flush is needed between steps.
+
+Metric: effective TFLOP/s = sum over linears of 6*M*N*K / step time (prep kernels included).
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl adahop|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica (the path is single-GPU); the
+reported value is the sum of work over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synthetic import WORKLOADS, tensor_recipes  # noqa: E402
+
+METRIC = "AdaHOP linear fwd+bwd eff. TFLOPS vs MXFP4 peak; prep-kernel HBM GB/s"
+WORKLOAD = "llama3.1-8b"
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor throughput on GB300
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+QUANT_BYTES_PER_ELEM = 2 + 0.5 + 1 / 32   # bf16 read + E2M1 write + E8M0 write
+
+
+# ------------------------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clocks and throttle reasons while GPU work is timed."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", self.gpu, "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        # "under load": samples drawing more than half the peak sampled power
+        loaded = [s for s, p in zip(sm, pw) if pw and p is not None and p > 0.5 * max(pw)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def cuda_time_ms(fn, reps: int, stream=None) -> float:
+    """Average device time of fn() over reps, CUDA events on the launching (current) stream."""
+    s = stream or torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(s)
+    for _ in range(reps):
+        fn()
+    end.record(s)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / reps
+
+
+# ------------------------------------------------------------------------------------ workload
+class LinearCase:
+    def __init__(self, q, wl, li, device):
+        lin = wl.linears[li]
+        self.name = lin.name
+        self.X, self.W, self.GY = tensor_recipes(wl, li, device=device)
+        self.M, self.K = self.X.shape
+        self.N = self.W.shape[0]
+        cal_ws = q.new_workspace(1 << 22, device=device)
+        self.plan = q.adahop_calibrate(self.X, self.W, self.GY, cal_ws)
+        self.Y = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=device)
+        self.dX = torch.empty((self.M, self.K), dtype=torch.bfloat16, device=device)
+        self.dW = torch.empty((self.N, self.K), dtype=torch.bfloat16, device=device)
+
+    def flops(self) -> int:
+        return 6 * self.M * self.N * self.K
+
+    def ws_bytes(self, q) -> int:
+        return q.adahop_workspace_size(self.plan, self.M, self.N, self.K)
+
+
+def launches_per_gemm(strategy: int, r: int, foid_shared: bool) -> int:
+    """Kernels the dispatcher launches for one GEMM (see the launch sequence in adahop.cu)."""
+    if strategy == 3:                       # BF16
+        return 1
+    if strategy in (1, 2) and r > 0:        # OE: FOID (2) + quantise (2) + ...
+        foid = 0 if foid_shared else 2
+        return foid + 2 + 3                 # inner: 2 gathers + GEMM; outer: gather + BF16 GEMM + scatter-add
+    return 3                                # quantise A, quantise B, GEMM
+
+
+class Bench:
+    def __init__(self, q, device):
+        self.q = q
+        self.device = device
+        self.wl = WORKLOADS[WORKLOAD]
+        self.cases = [LinearCase(q, self.wl, li, device) for li in range(len(self.wl.linears))]
+        self.ws = q.new_workspace(max(c.ws_bytes(q) for c in self.cases), device=device)
+        self.flops_per_step = sum(c.flops() for c in self.cases)
+
+    def step(self):
+        q = self.q
+        for c in self.cases:
+            q.adahop_linear_fwd(c.plan, c.X, c.W, c.Y, self.ws)
+            q.adahop_linear_bwd(c.plan, c.GY, c.X, c.W, c.dX, c.dW, self.ws)
+
+    def launches_per_step(self) -> int:
+        n = 0
+        for c in self.cases:
+            p = c.plan
+            n += launches_per_gemm(p.fwd, p.oe_rank, False)
+            same = p.dgrad in (1, 2) and p.dgrad == p.wgrad
+            n += launches_per_gemm(p.dgrad, p.oe_rank, False)
+            n += launches_per_gemm(p.wgrad, p.oe_rank, same)
+        return n
+
+    def strategies(self) -> dict:
+        from quantized_gemm_foid_gb300.binding import STRATEGY_NAMES, PATTERN_NAMES
+        p = self.cases[0].plan
+        return {"patterns": {"X": PATTERN_NAMES[p.x], "W": PATTERN_NAMES[p.w], "G_Y": PATTERN_NAMES[p.gy]},
+                "fwd": STRATEGY_NAMES[p.fwd], "dgrad": STRATEGY_NAMES[p.dgrad], "wgrad": STRATEGY_NAMES[p.wgrad],
+                "uniform_over_linears": all((c.plan.fwd, c.plan.dgrad, c.plan.wgrad) == (p.fwd, p.dgrad, p.wgrad)
+                                            for c in self.cases)}
+
+    # ------------------------------------------------------------------ dominant kernel (K3)
+    def gemm_roofline(self, reps: int = 3):
+        """Times the fused MXFP4 (+BF16 outlier) GEMM of every GEMM of one step on its own
+        (operands quantised once beforehand), CUDA events on the launching stream.
+        Returns (flops, seconds) summed over the step's GEMMs."""
+        q = self.q
+        tot_flops, tot_s, per = 0, 0.0, []
+        for c in self.cases:
+            p = c.plan
+            for gemm, strat in (("fwd", p.fwd), ("dgrad", p.dgrad), ("wgrad", p.wgrad)):
+                if strat not in (0, 1, 2, 4):
+                    continue
+                if gemm == "fwd":
+                    A, a_axis, B, b_axis, P, Q, J = c.X, 1, c.W, 1, c.M, c.N, c.K
+                elif gemm == "dgrad":
+                    A, a_axis, B, b_axis, P, Q, J = c.GY, 1, c.W, 0, c.M, c.K, c.N
+                else:
+                    A, a_axis, B, b_axis, P, Q, J = c.GY, 0, c.X, 0, c.N, c.K, c.M
+                inner = gemm == "wgrad" and strat in (1, 2) and p.oe_rank > 0
+                r = p.oe_rank if inner else 0
+                ac = torch.empty(P * J // 2, dtype=torch.uint8, device=self.device)
+                asf = torch.empty(P * J // 32, dtype=torch.uint8, device=self.device)
+                bc = torch.empty(Q * J // 2, dtype=torch.uint8, device=self.device)
+                bsf = torch.empty(Q * J // 32, dtype=torch.uint8, device=self.device)
+                q.adahop_quantize_mxfp4(A, a_axis, 1, None, None, ac, asf, 1)
+                q.adahop_quantize_mxfp4(B, b_axis, 1, None, None, bc, bsf, 1)
+                Ao = Bo = None
+                if r:
+                    Ao = torch.randn((P, r), device=self.device).to(torch.bfloat16)
+                    Bo = torch.randn((Q, r), device=self.device).to(torch.bfloat16)
+                out = c.Y if gemm == "fwd" else (c.dX if gemm == "dgrad" else c.dW)
+                ms = cuda_time_ms(lambda: q.adahop_gemm_mxfp4(ac, asf, bc, bsf, P, Q, J, Ao, Bo, r, out, self.ws),
+                                  reps)
+                f = 2 * P * Q * J + 2 * P * Q * r
+                tot_flops += f
+                tot_s += ms / 1e3
+                per.append({"linear": c.name, "gemm": gemm, "P": P, "Q": Q, "J": J, "r": r,
+                            "ms": round(ms, 4), "tflops": round(f / ms / 1e9, 1)})
+                del ac, asf, bc, bsf, Ao, Bo
+        return tot_flops, tot_s, per
+
+    def prep_bandwidth(self, reps: int = 5):
+        """Algorithmic-byte bandwidth of the IHT + MXFP4 quantiser on the largest operand
+        (G_Y of the gate projection), both orientations."""
+        q = self.q
+        c = max(self.cases, key=lambda c: c.M * c.N)
+        out = {}
+        for name, axis in (("rows", 1), ("cols", 0)):
+            n = c.M * c.N
+            codes = torch.empty(n // 2, dtype=torch.uint8, device=self.device)
+            sf = torch.empty(n // 32, dtype=torch.uint8, device=self.device)
+            ms = cuda_time_ms(lambda: q.adahop_quantize_mxfp4(c.GY, axis, 1, None, None, codes, sf, 1), reps)
+            out[name] = {"ms": round(ms, 4), "gbs": round(n * QUANT_BYTES_PER_ELEM / ms / 1e6, 1),
+                         "shape": [c.M, c.N]}
+        return out
+
+    # ------------------------------------------------------------------ end to end (host buffers)
+    def e2e(self, steps: int, warmup: int):
+        """Same metric through the C ABI with pinned host buffers: every step copies X, W, G_Y of
+        each linear host->device and Y, dX, dW device->host inside the timed region."""
+        q = self.q
+        host = []
+        for c in self.cases:
+            h = {k: getattr(c, k).cpu().pin_memory() for k in ("X", "W", "GY")}
+            h.update({k: torch.empty(getattr(c, k).shape, dtype=torch.bfloat16).pin_memory()
+                      for k in ("Y", "dX", "dW")})
+            host.append(h)
+        h2d = sum(h[k].numel() * 2 for h in host for k in ("X", "W", "GY"))
+        d2h = sum(h[k].numel() * 2 for h in host for k in ("Y", "dX", "dW"))
+
+        def one():
+            for c, h in zip(self.cases, host):
+                c.X.copy_(h["X"], non_blocking=True)
+                c.W.copy_(h["W"], non_blocking=True)
+                c.GY.copy_(h["GY"], non_blocking=True)
+                q.adahop_linear_fwd(c.plan, c.X, c.W, c.Y, self.ws)
+                q.adahop_linear_bwd(c.plan, c.GY, c.X, c.W, c.dX, c.dW, self.ws)
+                h["Y"].copy_(c.Y, non_blocking=True)
+                h["dX"].copy_(c.dX, non_blocking=True)
+                h["dW"].copy_(c.dW, non_blocking=True)
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        ms = cuda_time_ms(one, steps)
+        return ms, h2d, d2h
+
+
+# ------------------------------------------------------------------------------------ CPU oracle
+def oracle_sample_step(cache: dict) -> tuple[float, int]:
+    """One bounded sample of the workload through the CPU oracle: the first 256 tokens of the
+    k projection (N = 1024, K = 4096), Fwd + dgrad + wgrad with the calibrated strategies
+    (IHT, OE-Left outer, OE-Left inner; rank 64), quantisation included.  Returns (seconds, flops)."""
+    import oracle as O
+    from synthetic import bf16_bits
+    if "tensors" not in cache:
+        wl = WORKLOADS[WORKLOAD]
+        X, W, GY = tensor_recipes(wl, 1)           # CPU draw of the k projection's tensors
+        Ms = 256
+        cache["tensors"] = (bf16_bits(X[:Ms].contiguous()), bf16_bits(W), bf16_bits(GY[:Ms].contiguous()))
+        cache["plan"] = O.plan_from_patterns(O.PAT_COL, O.PAT_NONE, O.PAT_ROW, 64)
+    X, W, GY = cache["tensors"]
+    plan = cache["plan"]
+    t0 = time.perf_counter()
+    for gemm in O.GEMMS:
+        O.gemm_oracle(gemm, plan[gemm], X, W, GY, patterns=plan["patterns"], r=plan["oe_rank"])
+    dt = time.perf_counter() - t0
+    M, K = X.shape
+    N = W.shape[0]
+    return dt, 6 * M * N * K
+
+
+def cpu_baseline(budget_s: float = 12.0) -> dict:
+    cache, times, flops = {}, [], 0
+    oracle_sample_step(cache)                      # warm caches, draw the sample
+    t_end = time.perf_counter() + budget_s
+    while time.perf_counter() < t_end or not times:
+        dt, flops = oracle_sample_step(cache)
+        times.append(dt)
+    mean = sum(times) / len(times)
+    return {"value": flops / mean / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "first 256 tokens of the Llama3.1-8B k projection (N=1024, K=4096): Fwd IHT + dgrad "
+                      "OE-Left outer + wgrad OE-Left inner, rank 64, quantisation included; NumPy "
+                      f"(BLAS threads for the float64 products); mean of {len(times)} runs"}
+
+
+# ------------------------------------------------------------------------------------ main
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle as it stands, each step one bounded sample of the workload."""
+    if rank != 0:
+        return
+    cache = {}
+    for _ in range(args.warmup):
+        oracle_sample_step(cache)
+    times, flops = [], 0
+    for _ in range(args.steps):
+        dt, flops = oracle_sample_step(cache)
+        times.append(dt)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic",
+            "config": {"workload": "llama3.1-8b linear block fwd+bwd (bounded CPU sample per step)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": "first 256 tokens of the k projection, Fwd + dgrad + wgrad per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["adahop", "reference"], default="adahop")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import quantized_gemm_foid_gb300 as q
+
+    peaks, peak_kind = load_peaks()
+    b = Bench(q, device)
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+    sampler = ClockSampler(gpu_index)
+
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    st = q.adahop_get_device_status(b.ws)
+    if st != 0:
+        raise SystemExit(f"device status {st} after warm-up")
+
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    ms = cuda_time_ms(b.step, args.steps)
+    barrier(world)
+    ms = max_over_ranks(world, ms)
+    gflops, gsec, per_gemm = b.gemm_roofline()
+    prep = b.prep_bandwidth()
+    clocks = sampler.stop()
+    st = q.adahop_get_device_status(b.ws)
+    if st != 0:
+        raise SystemExit(f"device status {st} after the timed region")
+
+    e2e_ms, h2d, d2h = b.e2e(steps=3, warmup=1)
+    value = b.flops_per_step * world / (ms / 1e3) / 1e12
+
+    fp4_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * FP4_OVER_BF16
+    achieved = gflops / gsec / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1 x e2m1 (MXFP4) + bf16 outliers, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": "llama3.1-8b linear block fwd+bwd (q,k,v,o,gate,up,down)", "M": b.wl.M,
+                   "hidden": 4096, "kv": 1024, "ffn": 14336, "oe_rank": b.cases[0].plan.oe_rank,
+                   "strategies": b.strategies(), "outputs": "bf16",
+                   "l2": "no flush: every step reads and writes ~15 GB, >> 129 MB L2",
+                   "flops_per_step": b.flops_per_step},
+        "roofline": {"kernel": "fused MXFP4 + BF16-outlier tcgen05 GEMM", "bound": "tensor",
+                     "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
+                     "peak_source": f"{peak_kind}: bf16_tflops_sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
+                     "traffic": None, "launches": len(per_gemm)},
+        "prep": {"kernel": "IHT + MXFP4 quantiser", "bound": "hbm", "peak_gbs": peaks.get("hbm_gbs"),
+                 **{k: dict(v, frac=round(v["gbs"] / peaks.get("hbm_gbs", 6800.0), 3)) for k, v in prep.items()}},
+        "gemms": per_gemm,
+        "clocks": clocks,
+        "e2e": {"value": b.flops_per_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": b.launches_per_step() * args.steps,
+    }
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
