@@ -187,8 +187,9 @@ adahop_status adahop_gemm_mxfp4(const uint8_t *a_codes, const uint8_t *a_scales,
 /* BF16 GEMM C (P x Q) = A . B, float32 accumulation (Fig. 5's BF16 path; also the outlier
  * GEMM of outer OE).  a_kmajor 1: A stored P x J (J-contiguous); 0: stored J x P.
  * b_kmajor 1: B stored Q x J (i.e. B^T row-major); 0: stored J x Q.
- * splits > 1 (only with c_partial): J is cut into `splits` ranges and partial sums go to
- * c_partial[s] (fp32, splits x P x Q) instead of C.  P >= 1 (a multiple of 64 when A is
+ * With c_partial non-NULL, J is cut into `splits` (>= 1) ranges and the partial sums go to
+ * c_partial[s] (fp32, splits x P x Q) instead of C (C may then be NULL; splits > 1 requires
+ * c_partial).  P >= 1 (a multiple of 64 when A is
  * stored J x P); Q and J multiples of 64.  The workspace only carries the status word. */
 adahop_status adahop_gemm_bf16(const void *A, int a_kmajor, const void *B, int b_kmajor,
                                int64_t P, int64_t Q, int64_t J, void *C, int out_dtype,

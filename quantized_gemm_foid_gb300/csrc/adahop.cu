@@ -229,6 +229,7 @@ struct Ctx {
 adahop_status bf16_gemm(const Ctx &cx, const void *A, int a_kmajor, const void *B, int b_kmajor,
                         int64_t P, int64_t Q, int64_t J, void *C, int out_dtype, int splits,
                         float *partial) {
+  if (!partial && !C) return ADAHOP_ERR_INVALID_ARG;
   GemmMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   if (a_kmajor)
@@ -647,7 +648,7 @@ adahop_status adahop_gemm_bf16(const void *A, int a_kmajor, const void *B, int b
                                size_t ws_bytes, adahop_stream_t stream) {
   if (!A || !B || !workspace || (a_kmajor != 0 && a_kmajor != 1) || (b_kmajor != 0 && b_kmajor != 1))
     return ADAHOP_ERR_INVALID_ARG;
-  if (splits < 1 || splits > 64 || (splits > 1 && !c_partial) || (splits == 1 && !C)) return ADAHOP_ERR_INVALID_ARG;
+  if (splits < 1 || splits > 64 || (splits > 1 && !c_partial) || (!c_partial && !C)) return ADAHOP_ERR_INVALID_ARG;
   if (out_dtype != 0 && out_dtype != 1) return ADAHOP_ERR_INVALID_ARG;
   if (P <= 0 || Q <= 0 || J <= 0 || Q % 64 || J % 64) return ADAHOP_ERR_SHAPE;
   if (!a_kmajor && P % 64) return ADAHOP_ERR_SHAPE;

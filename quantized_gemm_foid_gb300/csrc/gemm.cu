@@ -288,6 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ epilogue warps
     const int quad = warp & 3;                        // TMEM lanes 32*quad .. 32*quad+31
     const int half = (warp - 2) >> 2;                 // accumulator columns 128*half ..
+    // Partial mode (split-K or not) is chosen by a non-null c_partial; with neither output the
+    // tiles are computed but nothing is stored and the status word records the bad argument.
+    const bool to_partial = g.c_partial != nullptr;
+    const bool can_store = to_partial || g.C != nullptr;
+    if (!can_store && threadIdx.x == 64) report_status(g.status, kStatusBadArg);
     uint32_t acc_phase = 0;
     for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest);
@@ -313,15 +318,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc_phase ^= 1u;
 
       const int64_t row = t.m0 + 32 * quad + lane;
-      if (row < g.P) {
+      if (can_store && row < g.P) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int64_t col = t.n0 + 128 * half + 32 * j;
           if (col >= g.Q) continue;
           const bool full = col + 32 <= g.Q;
-          if (g.splits > 1 || g.out_dtype == 1) {
-            float *dst = (g.splits > 1 ? g.c_partial + static_cast<int64_t>(t.split) * g.P * g.Q
-                                       : static_cast<float *>(g.C)) +
+          if (to_partial || g.out_dtype == 1) {
+            float *dst = (to_partial ? g.c_partial + static_cast<int64_t>(t.split) * g.P * g.Q
+                                     : static_cast<float *>(g.C)) +
                          row * g.Q + col;
             if (full) {
 #pragma unroll

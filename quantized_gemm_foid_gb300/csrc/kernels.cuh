@@ -50,8 +50,8 @@ struct GemmArgs {
   int tail_stages;            // MXFP4: ceil(r / 64) stages of BF16 outlier MMAs
   void *C;
   int out_dtype;              // 0 bf16, 1 fp32
-  int splits;                 // BF16: split-K count (partials go to c_partial)
-  float *c_partial;
+  int splits;                 // BF16: split-K count (>= 1)
+  float *c_partial;           // non-null: fp32 partials (splits x P x Q) are written here, not C
   uint32_t *status;
 };
 struct GemmMaps {

@@ -15,15 +15,17 @@ namespace {
 
 // ------------------------------------------------------------------------------- gathers
 // mode 0: out[i, :] = T[idx[i], :]   (r x cols), 16-byte copies
-__global__ void gather_rows_kernel(const uint16_t *__restrict__ T, int64_t cols,
+__global__ void gather_rows_kernel(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
                                    const int32_t *__restrict__ idx, int r, uint16_t *out) {
   const int64_t vec = cols >> 3;
   const int64_t total = static_cast<int64_t>(r) * vec;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t i = t / vec, v = t - i * vec;
+    const int64_t src = idx[i];
+    if (src < 0 || src >= rows) continue;        // indices come from FOID; never read outside T
     reinterpret_cast<uint4 *>(out + i * cols)[v] =
-        __ldg(reinterpret_cast<const uint4 *>(T + static_cast<int64_t>(idx[i]) * cols) + v);
+        __ldg(reinterpret_cast<const uint4 *>(T + src * cols) + v);
   }
 }
 // mode 1: out[p, i] = T[p, idx[i]]   (rows x r)
@@ -33,17 +35,19 @@ __global__ void gather_cols_kernel(const uint16_t *__restrict__ T, int64_t rows,
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t p = t / r, i = t - p * r;
-    out[t] = __ldg(T + p * cols + idx[i]);
+    const int64_t c = idx[i];
+    out[t] = (c >= 0 && c < cols) ? __ldg(T + p * cols + c) : static_cast<uint16_t>(0);
   }
 }
 // mode 2: out[q, i] = T[idx[i], q]   (cols x r): a 32-column x r tile through shared memory
-__global__ void gather_rows_t_kernel(const uint16_t *__restrict__ T, int64_t cols,
+__global__ void gather_rows_t_kernel(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
                                      const int32_t *__restrict__ idx, int r, uint16_t *out) {
   __shared__ uint16_t tile[256][34];
   const int64_t q0 = static_cast<int64_t>(blockIdx.x) * 32;
   for (int t = threadIdx.x; t < r * 32; t += blockDim.x) {
     const int i = t >> 5, q = t & 31;
-    tile[i][q] = __ldg(T + static_cast<int64_t>(idx[i]) * cols + q0 + q);
+    const int64_t src = idx[i];
+    tile[i][q] = (src >= 0 && src < rows) ? __ldg(T + src * cols + q0 + q) : static_cast<uint16_t>(0);
   }
   __syncthreads();
   for (int t = threadIdx.x; t < r * 32; t += blockDim.x) {
@@ -58,7 +62,8 @@ __global__ void gather_cols_t_kernel(const uint16_t *__restrict__ T, int64_t row
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t i = t / rows, p = t - i * rows;
-    out[t] = __ldg(T + p * cols + idx[i]);
+    const int64_t c = idx[i];
+    out[t] = (c >= 0 && c < cols) ? __ldg(T + p * cols + c) : static_cast<uint16_t>(0);
   }
 }
 
@@ -72,15 +77,17 @@ __device__ __forceinline__ void store_out(uint16_t *p, float v) {
 
 // axis 0: C[idx[i], q] += sum_s partial[s, i, q]
 template <typename OutT>
-__global__ void scatter_rows_kernel(OutT *C, int64_t Q, const float *__restrict__ partial,
+__global__ void scatter_rows_kernel(OutT *C, int64_t P, int64_t Q, const float *__restrict__ partial,
                                     int splits, const int32_t *__restrict__ idx, int r) {
   const int64_t total = static_cast<int64_t>(r) * Q;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t i = t / Q, q = t - i * Q;
     float acc = 0.0f;
+    const int64_t row = idx[i];
+    if (row < 0 || row >= P) continue;           // never write outside C
     for (int s = 0; s < splits; ++s) acc += partial[s * total + t];
-    OutT *dst = C + static_cast<int64_t>(idx[i]) * Q + q;
+    OutT *dst = C + row * Q + q;
     store_out(dst, load_out(dst) + acc);
   }
 }
@@ -93,8 +100,10 @@ __global__ void scatter_cols_kernel(OutT *C, int64_t P, int64_t Q, const float *
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t p = t / r, i = t - p * r;
     float acc = 0.0f;
+    const int64_t col = idx[i];
+    if (col < 0 || col >= Q) continue;           // never write outside C
     for (int s = 0; s < splits; ++s) acc += partial[s * total + t];
-    OutT *dst = C + p * Q + idx[i];
+    OutT *dst = C + p * Q + col;
     store_out(dst, load_out(dst) + acc);
   }
 }
@@ -160,13 +169,13 @@ cudaError_t launch_gather(const uint16_t *T, int64_t rows, int64_t cols, const i
   if (r == 0) return cudaSuccess;
   switch (mode) {
     case 0:
-      gather_rows_kernel<<<grid_for(r * (cols >> 3), 256), 256, 0, s>>>(T, cols, idx, r, out);
+      gather_rows_kernel<<<grid_for(r * (cols >> 3), 256), 256, 0, s>>>(T, rows, cols, idx, r, out);
       break;
     case 1:
       gather_cols_kernel<<<grid_for(rows * r, 256), 256, 0, s>>>(T, rows, cols, idx, r, out);
       break;
     case 2:
-      gather_rows_t_kernel<<<static_cast<unsigned>(cols / 32), 256, 0, s>>>(T, cols, idx, r, out);
+      gather_rows_t_kernel<<<static_cast<unsigned>(cols / 32), 256, 0, s>>>(T, rows, cols, idx, r, out);
       break;
     case 3:
       gather_cols_t_kernel<<<grid_for(rows * r, 256), 256, 0, s>>>(T, rows, cols, idx, r, out);
@@ -184,9 +193,9 @@ cudaError_t launch_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype, con
   const unsigned g = grid_for(work, 256);
   if (axis == 0) {
     if (out_dtype == 1)
-      scatter_rows_kernel<float><<<g, 256, 0, s>>>(static_cast<float *>(C), Q, partial, splits, idx, r);
+      scatter_rows_kernel<float><<<g, 256, 0, s>>>(static_cast<float *>(C), P, Q, partial, splits, idx, r);
     else
-      scatter_rows_kernel<uint16_t><<<g, 256, 0, s>>>(static_cast<uint16_t *>(C), Q, partial, splits,
+      scatter_rows_kernel<uint16_t><<<g, 256, 0, s>>>(static_cast<uint16_t *>(C), P, Q, partial, splits,
                                                       idx, r);
   } else {
     if (out_dtype == 1)
