@@ -142,14 +142,38 @@ class LinearCase:
         return q.adahop_workspace_size(self.plan, self.M, self.N, self.K)
 
 
-def launches_per_gemm(strategy: int, r: int, foid_shared: bool) -> int:
-    """Kernels the dispatcher launches for one GEMM (see the launch sequence in adahop.cu)."""
-    if strategy == 3:                       # BF16
+# Geometry of an extracted line (the dispatcher's table): which of P (rows of C), Q (columns of
+# C) or J (inner) a source tensor's rows / columns are in each GEMM.
+_AXIS_ROLE = {
+    "fwd": {"X": ("P", "J"), "W": ("Q", "J")},
+    "dgrad": {"GY": ("P", "J"), "W": ("J", "Q")},
+    "wgrad": {"GY": ("J", "P"), "X": ("J", "Q")},
+}
+_SOURCES = {"fwd": ("X", "W"), "dgrad": ("GY", "W"), "wgrad": ("GY", "X")}
+
+
+def oe_source(gemm: str, strategy: int, pats: dict):
+    """(tensor, axis) that OE-Left (rows of the Row-wise operand, else the A-source) or OE-Right
+    (columns of the Column-wise operand, else the B-source) extracts."""
+    a, b = _SOURCES[gemm]
+    if strategy == 1:
+        rows = [t for t in (a, b) if pats[t] == 1]
+        return (rows[0] if len(rows) == 1 else a), 0
+    cols = [t for t in (a, b) if pats[t] == 2]
+    return (cols[0] if len(cols) == 1 else b), 1
+
+
+def launches_per_gemm(gemm: str, strategy: int, r: int, pats: dict, foid_shared: bool) -> int:
+    """Kernels the dispatcher launches for one GEMM (the launch sequence of adahop.cu)."""
+    if strategy == 3:                        # BF16: one GEMM
         return 1
-    if strategy in (1, 2) and r > 0:        # OE: FOID (2) + quantise (2) + ...
-        foid = 0 if foid_shared else 2
-        return foid + 2 + 3                 # inner: 2 gathers + GEMM; outer: gather + BF16 GEMM + scatter-add
-    return 3                                # quantise A, quantise B, GEMM
+    if strategy in (1, 2) and r > 0:
+        t, axis = oe_source(gemm, strategy, pats)
+        role = _AXIS_ROLE[gemm][t][axis]
+        foid = 0 if foid_shared else 2       # local top-r + merge
+        # quantise A, B; inner: gather A_o, B_o + fused GEMM; outer: GEMM + gather + BF16 GEMM + scatter-add
+        return foid + 2 + (3 if role == "J" else 4)
+    return 3                                 # quantise A, quantise B, GEMM
 
 
 class Bench:
@@ -171,10 +195,12 @@ class Bench:
         n = 0
         for c in self.cases:
             p = c.plan
-            n += launches_per_gemm(p.fwd, p.oe_rank, False)
-            same = p.dgrad in (1, 2) and p.dgrad == p.wgrad
-            n += launches_per_gemm(p.dgrad, p.oe_rank, False)
-            n += launches_per_gemm(p.wgrad, p.oe_rank, same)
+            pats = {"X": p.x, "W": p.w, "GY": p.gy}
+            n += launches_per_gemm("fwd", p.fwd, p.oe_rank, pats, False)
+            n += launches_per_gemm("dgrad", p.dgrad, p.oe_rank, pats, False)
+            shared = (p.dgrad in (1, 2) and p.wgrad in (1, 2) and p.oe_rank > 0 and
+                      oe_source("dgrad", p.dgrad, pats) == oe_source("wgrad", p.wgrad, pats))
+            n += launches_per_gemm("wgrad", p.wgrad, p.oe_rank, pats, shared)
         return n
 
     def strategies(self) -> dict:
@@ -360,12 +386,46 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def profile(q, device, args):
+    """Workloads for the committed ncu summaries (profiles/); no timing, no bench line."""
+    if args.profile == "step":
+        b = Bench(q, device)
+        for _ in range(args.warmup):
+            b.step()
+        b.step()
+        torch.cuda.synchronize()
+        assert q.adahop_get_device_status(b.ws) == 0
+        print(f"profiled one step: {b.launches_per_step()} launches")
+        return
+    from synthetic import normal_bf16
+    P, Q, J = 32768, 4096, 14336
+    A = normal_bf16(P, J, 1e-3, 1, device=device)
+    B = normal_bf16(J, Q, 0.02, 2, device=device)      # W (N x K), quantised along N
+    ac = torch.empty(P * J // 2, dtype=torch.uint8, device=device)
+    asf = torch.empty(P * J // 32, dtype=torch.uint8, device=device)
+    bc = torch.empty(Q * J // 2, dtype=torch.uint8, device=device)
+    bsf = torch.empty(Q * J // 32, dtype=torch.uint8, device=device)
+    q.adahop_quantize_mxfp4(A, 1, 1, None, None, ac, asf, 1)
+    q.adahop_quantize_mxfp4(B, 0, 1, None, None, bc, bsf, 1)
+    C = torch.empty((P, Q), dtype=torch.bfloat16, device=device)
+    ws = q.new_workspace(4096, device=device)
+    for _ in range(3):
+        q.adahop_gemm_mxfp4(ac, asf, bc, bsf, P, Q, J, None, None, 0, C, ws)
+    torch.cuda.synchronize()
+    assert q.adahop_get_device_status(ws) == 0
+    print("profiled 3 fused MXFP4 GEMM launches")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["adahop", "reference"], default="adahop")
+    ap.add_argument("--profile", choices=["step", "gemm"], default=None,
+                    help="for ncu only (prints no bench line): 'step' = warm-up steps then one step "
+                         "of the workload; 'gemm' = three launches of the fused MXFP4 GEMM on the "
+                         "dgrad shape P=32768, Q=4096, J=14336")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -377,6 +437,9 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     import quantized_gemm_foid_gb300 as q
+    if args.profile:
+        profile(q, device, args)
+        return
 
     peaks, peak_kind = load_peaks()
     b = Bench(q, device)
