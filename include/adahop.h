@@ -144,6 +144,24 @@ adahop_status adahop_foid(const void *T, int64_t rows, int64_t cols, int axis, i
                           size_t ws_bytes, adahop_stream_t stream);
 size_t adahop_foid_workspace_size(int64_t lines, int r);
 
+/* FOID without a workspace.  The paper has no counterpart to this entry point: it exists for
+ * callers that cannot allocate device memory -- code that is handed only its inputs and outputs
+ * (a plug-in or callback inside another runtime that owns all device memory) or that must not
+ * call cudaMalloc (it may synchronise the device and can fail at run time).  It computes exactly
+ * what adahop_foid computes (same arguments and results, minus the workspace) and allocates
+ * nothing: its scratch is a fixed 64 KB device array inside the library (8192 candidate keys),
+ * held by every GPU that loads the library until the process exits.
+ *   - Limit: ceil(lines / 2048) * r must be <= 8192 (e.g. r = 256 for up to 65536 lines);
+ *     larger requests return ADAHOP_ERR_SHAPE before anything is launched.
+ *   - The first call on a device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (nothing in it needs to
+ *     start at zero).  Calls whose kernels overlap on the GPU (e.g. on different streams) race
+ *     on it and must be serialised by the caller. */
+adahop_status adahop_foid_noalloc(const void *T, int64_t rows, int64_t cols, int axis, int r,
+                                  int32_t *idx_out, uint32_t *line_mask_out,
+                                  adahop_stream_t stream);
+
 /* IHT + MXFP4 quantisation (appendix, IHT and Quantization: 1D FWHT with block size 32 on
  * the residual, then MXFP4 with 1D scaling).
  * T: rows x cols bf16.  inner_axis 1: quantise along the columns (output lines = rows,

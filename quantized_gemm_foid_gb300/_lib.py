@@ -45,6 +45,8 @@ PROTOTYPES = {
     "adahop_foid": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p,
                             c_void_p, c_size_t, c_void_p]),
     "adahop_foid_workspace_size": (c_size_t, [c_int64, c_int]),
+    "adahop_foid_noalloc": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p,
+                                    c_void_p]),
     "adahop_quantize_mxfp4": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p,
                                       c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "adahop_gather": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_int, c_int, c_void_p,

@@ -148,6 +148,15 @@ def adahop_foid(T, axis: int, r: int, idx_out, mask_out, workspace, stream=None)
                            workspace.numel(), _stream(stream)), "adahop_foid")
 
 
+def adahop_foid_noalloc(T, axis: int, r: int, idx_out, mask_out, stream=None) -> None:
+    """FOID for callers that cannot allocate: the library keeps the scratch in a fixed device
+    array (up to ceil(lines / 2048) * r = 8192 candidates); concurrent calls race on it."""
+    _cuda(T, "T", torch.bfloat16)
+    rows, cols = T.shape
+    _check(LIB.adahop_foid_noalloc(_p(T), rows, cols, axis, r, _p(idx_out), _p(mask_out), _stream(stream)),
+           "adahop_foid_noalloc")
+
+
 def adahop_quantize_mxfp4(T, inner_axis: int, hadamard: int, zero_rows_mask, zero_cols_mask, codes,
                           scales, scale_layout: int = 0, stream=None) -> None:
     _cuda(T, "T", torch.bfloat16)

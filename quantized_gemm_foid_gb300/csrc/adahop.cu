@@ -593,6 +593,23 @@ adahop_status adahop_foid(const void *T, int64_t rows, int64_t cols, int axis, i
   return ADAHOP_OK;
 }
 
+adahop_status adahop_foid_noalloc(const void *T, int64_t rows, int64_t cols, int axis, int r, int32_t *idx_out,
+                                  uint32_t *line_mask_out, adahop_stream_t stream) {
+  if (!T || (!idx_out && r > 0) || (axis != 0 && axis != 1)) return ADAHOP_ERR_INVALID_ARG;
+  if (rows < 64 || cols < 64 || (axis == 0 && cols % 8)) return ADAHOP_ERR_SHAPE;
+  const int64_t lines = axis == 0 ? rows : cols;
+  if (r < 0 || r > kMaxRank || r > lines) return ADAHOP_ERR_SHAPE;
+  // the candidates of stage 1 must fit the fixed device array
+  if ((lines + 2047) / 2048 * static_cast<int64_t>(r) > foid_static_capacity()) return ADAHOP_ERR_SHAPE;
+  if (!aligned(T, 16)) return ADAHOP_ERR_ALIGN;
+  DeviceInfo di;
+  ST_TRY(device_info(&di));
+  CUDA_TRY(launch_foid_noalloc(static_cast<const uint16_t *>(T), rows, cols, axis, r, idx_out, line_mask_out,
+                               reinterpret_cast<cudaStream_t>(stream)),
+           "foid (no workspace)");
+  return ADAHOP_OK;
+}
+
 adahop_status adahop_quantize_mxfp4(const void *T, int64_t rows, int64_t cols, int inner_axis, int hadamard,
                                     const uint32_t *zero_rows_mask, const uint32_t *zero_cols_mask, uint8_t *codes,
                                     uint8_t *scales, int scale_layout, adahop_stream_t stream) {

@@ -13,6 +13,8 @@
 // Stage 1 (grid): each CTA scores 2048 lines (512 threads x 4), sorts their keys in shared
 // memory (bitonic) and writes its best r.  Stage 2 (one CTA): sorts the candidates, keeps the
 // best r, writes their indices in ascending order and the bitmap of selected lines.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -182,6 +184,55 @@ cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis,
   foid_merge_kernel<<<1, 1024, smem, s>>>(cand, static_cast<int>(ncand), np2, r, lines, idx_out,
                                           mask_out);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// FOID for callers that cannot hand the library any scratch memory.
+//
+// Some callers only own their inputs and outputs: a plug-in or callback running inside another
+// runtime that manages all device memory itself, or a code path that must not call cudaMalloc
+// (it can synchronise the device and fail at run time).  For them the candidate keys of stage 1
+// live in the fixed array below instead of a workspace.  It holds kFoidStaticKeys = 8192 keys
+// (64 KB), the same ceiling the merge stage already has, on every GPU that loads the library,
+// for the life of the process.  Stage 1 writes every slot that stage 2 reads, so nothing in it
+// has to start at zero; it keeps whatever the last call wrote.  All calls share it: two calls
+// whose kernels overlap on the GPU (e.g. on two streams) race on it.
+// ---------------------------------------------------------------------------------------------
+constexpr int kFoidStaticKeys = kFoidMergeMaxKeys;
+static __device__ __align__(256) uint64_t g_foid_static_keys[kFoidStaticKeys];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_keys_mutex;
+void *g_static_keys_addr[kMaxDevices] = {};   // device address of the array, per device
+
+// The array's name is only a host-side stand-in; its device address comes from the runtime,
+// looked up once per device with that device current.
+cudaError_t static_keys_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_keys_mutex);
+  if (!g_static_keys_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_foid_static_keys);
+    if (e != cudaSuccess) return e;
+    g_static_keys_addr[dev] = p;
+  }
+  *out = g_static_keys_addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+int64_t foid_static_capacity() { return kFoidStaticKeys; }
+
+cudaError_t launch_foid_noalloc(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
+                                int32_t *idx_out, uint32_t *mask_out, cudaStream_t s) {
+  void *keys = nullptr;
+  cudaError_t e = static_keys_address(&keys);
+  if (e != cudaSuccess) return e;
+  return launch_foid(T, rows, cols, axis, r, idx_out, mask_out, keys, s);
 }
 
 }  // namespace adahop

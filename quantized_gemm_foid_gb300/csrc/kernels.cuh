@@ -32,6 +32,11 @@ size_t foid_scratch_bytes(int64_t lines, int r);
 cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
                         int32_t *idx_out, uint32_t *mask_out, void *scratch, cudaStream_t s);
 
+// FOID with its candidate keys in a fixed device array instead of caller scratch (see foid.cu).
+int64_t foid_static_capacity();
+cudaError_t launch_foid_noalloc(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
+                                int32_t *idx_out, uint32_t *mask_out, cudaStream_t s);
+
 cudaError_t launch_gather(const uint16_t *T, int64_t rows, int64_t cols, const int32_t *idx, int r,
                           int mode, uint16_t *out, cudaStream_t s);
 
