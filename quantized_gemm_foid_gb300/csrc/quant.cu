@@ -11,15 +11,17 @@
 //     float32; then x * c with c = float32 nearest 1/sqrt(32) (0x3E3504F3);
 //   * amax = max |x| over the block; E8M0 byte = clamp(floor(log2 amax) - 2 + 127, 0, 254),
 //     floor(log2) read from the exponent bits (subnormals via the leading mantissa bit);
-//   * v = |x| * 2^(127 - byte) (exact power-of-two scaling); the E2M1 magnitude index is
-//     counted from the midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 with ties to the even
-//     index (strict > before odd indices, >= before even ones); values above 5 saturate to 6;
-//   * sign bit = the element's sign bit; an all-zero block stores byte 0 and codes 0.
-// Two orientations:
-//   rows kernel: J = columns (J-contiguous input); 4 threads per 32-block, 8 elements each,
-//                the strides 8 and 16 of the butterfly across lanes via warp shuffles;
-//   cols kernel: J = rows (the transposed orientation); a 128 x 128 tile is staged in shared
-//                memory and every thread transforms two 32-blocks of one column in registers.
+//   * v = x * 2^(127 - byte) (exact power-of-two scaling, |v| < 8); the E2M1 code is v rounded
+//     to the nearest E2M1 value, ties to the even code, saturating at 6, sign from v (so -0 and
+//     negative values that round to zero give 0x8) -- exactly what cvt.rn.satfinite.e2m1x2.f32
+//     computes, two elements per instruction;
+//   * an all-zero block stores byte 0 and codes 0.
+// Work distribution (HBM-bound: 2 B read + 0.53 B written per element):
+//   rows kernel: J = columns.  One thread per 32-block: four 16-byte loads, all five butterfly
+//                stages in registers, one 16-byte code store (a warp stores 512 contiguous bytes).
+//   cols kernel: J = rows (the transposed orientation).  A 128 x 128 tile is staged in shared
+//                memory; each thread reads a column pair as 32-bit words and transforms one
+//                32-row block of both columns in registers.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -51,13 +53,19 @@ __device__ __forceinline__ float mx_inv_scale(uint32_t byte) {
   return __uint_as_float((254u - byte) << 23);
 }
 
-__device__ __forceinline__ uint32_t e2m1_code(float x, float inv_s) {
-  const float v = __fmul_rn(fabsf(x), inv_s);
-  const uint32_t m = static_cast<uint32_t>(v > 0.25f) + static_cast<uint32_t>(v >= 0.75f) +
-                     static_cast<uint32_t>(v > 1.25f) + static_cast<uint32_t>(v >= 1.75f) +
-                     static_cast<uint32_t>(v > 2.5f) + static_cast<uint32_t>(v >= 3.5f) +
-                     static_cast<uint32_t>(v > 5.0f);
-  return m | ((__float_as_uint(x) >> 28) & 8u);
+// Eight scaled elements -> eight E2M1 codes, element i in bits 4i..4i+3.
+__device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4,
+                                           float v5, float v6, float v7) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return out;
 }
 
 __device__ __forceinline__ void butterfly(float &a, float &b) {
@@ -67,184 +75,162 @@ __device__ __forceinline__ void butterfly(float &a, float &b) {
   b = d;
 }
 
-// In-thread butterflies with stride H over N consecutive elements (N a multiple of 2H).
-template <int N, int H>
-__device__ __forceinline__ void butterfly_stage(float (&x)[N]) {
+// The orthonormal block-32 Sylvester Hadamard in place (stride 1, 2, 4, 8, 16, then scale).
+__device__ __forceinline__ void fwht32(float (&x)[32]) {
 #pragma unroll
-  for (int i = 0; i < N; ++i) {
-    if ((i & H) == 0) butterfly(x[i], x[i + H]);
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((i & h) == 0) butterfly(x[i], x[i + h]);
   }
+  const float c = inv_sqrt32();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], c);
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &raw, float (&x)[8]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    x[2 * k] = bf16_bits_to_f32(w[k] & 0xFFFFu);
-    x[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
-  }
-}
-
-__device__ __forceinline__ void store_scale(uint8_t *scales, int layout, int64_t line, int64_t blk,
-                                            int64_t J, uint32_t byte) {
-  const int64_t off = layout == 0 ? line * (J >> 5) + blk : tiled_sf_offset(line, blk, J);
-  scales[off] = static_cast<uint8_t>(byte);
-}
-
-// ---------------------------------------------------------------------------------------------
-// rows kernel: lines = rows of T, J = cols.
-// ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void quant_rows_chunk(const QuantArgs &a, int64_t chunk, uint4 raw,
-                                                 uint32_t gmask, int sub) {
-  const int64_t J = a.cols;
-  const int64_t cpr = J >> 3;                  // 8-element chunks per row
-  const int64_t row = chunk / cpr;
-  const int64_t col0 = (chunk - row * cpr) << 3;
-  float x[8];
-  unpack8(raw, x);
-  bool zero_all = false;
-  if (a.zero_rows) zero_all = (a.zero_rows[row >> 5] >> (row & 31)) & 1u;
-  uint32_t zc = 0;
-  if (a.zero_cols) zc = (a.zero_cols[col0 >> 5] >> (col0 & 31)) & 0xFFu;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (zero_all || ((zc >> i) & 1u)) x[i] = 0.0f;
-  }
-  if (a.hadamard) {
-    butterfly_stage<8, 1>(x);
-    butterfly_stage<8, 2>(x);
-    butterfly_stage<8, 4>(x);
-    // stride 8: partner lane sub ^ 1; the lower element keeps a + b, the upper b' = a - b
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float y = __shfl_xor_sync(gmask, x[i], 1);
-      x[i] = (sub & 1) ? __fsub_rn(y, x[i]) : __fadd_rn(x[i], y);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float y = __shfl_xor_sync(gmask, x[i], 2);
-      x[i] = (sub & 2) ? __fsub_rn(y, x[i]) : __fadd_rn(x[i], y);
-    }
-    const float c = inv_sqrt32();
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], c);
-  }
+// Quantises one 32-block in registers: returns the scale byte and writes 16 code bytes.
+__device__ __forceinline__ uint32_t quantize_block(float (&x)[32], uint4 &codes) {
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
   const uint32_t byte = mx_scale_byte(amax);
-  uint32_t word = 0;
   if (amax > 0.0f) {
-    const float inv_s = mx_inv_scale(byte);
+    const float s = mx_inv_scale(byte);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) word |= e2m1_code(x[i], inv_s) << (4 * i);
+    for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], s);
+    codes.x = e2m1x8(x[0], x[1], x[2], x[3], x[4], x[5], x[6], x[7]);
+    codes.y = e2m1x8(x[8], x[9], x[10], x[11], x[12], x[13], x[14], x[15]);
+    codes.z = e2m1x8(x[16], x[17], x[18], x[19], x[20], x[21], x[22], x[23]);
+    codes.w = e2m1x8(x[24], x[25], x[26], x[27], x[28], x[29], x[30], x[31]);
+  } else {
+    codes = make_uint4(0u, 0u, 0u, 0u);
   }
-  *reinterpret_cast<uint32_t *>(a.codes + row * (J >> 1) + (col0 >> 1)) = word;
-  if (sub == 0) store_scale(a.scales, a.scale_layout, row, col0 >> 5, J, byte);
+  return byte;
+}
+
+__device__ __forceinline__ int64_t scale_offset(int layout, int64_t line, int64_t blk, int64_t J) {
+  return layout == 0 ? line * (J >> 5) + blk : tiled_sf_offset(line, blk, J);
+}
+
+// ---------------------------------------------------------------------------------------------
+// rows kernel: lines = rows of T, J = cols; one thread per 32-block.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void quant_rows_block(const QuantArgs &a, int64_t blkid, const uint4 (&raw)[4]) {
+  const int64_t J = a.cols;
+  const int64_t bpr = J >> 5;                  // 32-blocks per row
+  const int64_t row = blkid / bpr;
+  const int64_t blk = blkid - row * bpr;
+  float x[32];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[8 * k + 2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
+      x[8 * k + 2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
+    }
+  }
+  uint32_t zmask = 0;
+  if (a.zero_rows && ((a.zero_rows[row >> 5] >> (row & 31)) & 1u)) zmask = 0xFFFFFFFFu;
+  if (a.zero_cols) zmask |= a.zero_cols[blk];          // bits of columns 32*blk .. 32*blk+31
+  if (zmask) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((zmask >> i) & 1u) x[i] = 0.0f;
+  }
+  if (a.hadamard) fwht32(x);
+  uint4 codes;
+  const uint32_t byte = quantize_block(x, codes);
+  *reinterpret_cast<uint4 *>(a.codes + row * (J >> 1) + (blk << 4)) = codes;
+  a.scales[scale_offset(a.scale_layout, row, blk, J)] = static_cast<uint8_t>(byte);
 }
 
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantArgs a) {
-  const int64_t total = a.rows * (a.cols >> 3);
-  const int lane = threadIdx.x & 31;
-  const int sub = lane & 3;
-  const uint32_t gmask = 0xFu << (lane & ~3);
+  const int64_t total = a.rows * (a.cols >> 5);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const uint4 *src = reinterpret_cast<const uint4 *>(a.T);
-  // Two independent chunks in flight per thread.  The four lanes of one 32-block always take
-  // the same branch: their chunk indices are 4q..4q+3, and total and stride are multiples of 4.
-  for (; c + stride < total; c += 2 * stride) {
-    const uint4 r0 = __ldg(src + c);
-    const uint4 r1 = __ldg(src + c + stride);
-    quant_rows_chunk(a, c, r0, gmask, sub);
-    quant_rows_chunk(a, c + stride, r1, gmask, sub);
+  // two blocks (128 bytes) in flight per thread
+  for (; b + stride < total; b += 2 * stride) {
+    uint4 r0[4], r1[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) r0[k] = __ldg(src + 4 * b + k);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) r1[k] = __ldg(src + 4 * (b + stride) + k);
+    quant_rows_block(a, b, r0);
+    quant_rows_block(a, b + stride, r1);
   }
-  if (c < total) quant_rows_chunk(a, c, __ldg(src + c), gmask, sub);
+  if (b < total) {
+    uint4 r0[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) r0[k] = __ldg(src + 4 * b + k);
+    quant_rows_block(a, b, r0);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
-// cols kernel: lines = columns of T, J = rows.  Tile 128 rows x 128 cols, 256 threads.
+// cols kernel: lines = columns of T, J = rows.  Tile 128 rows x 128 cols, 256 threads; thread t
+// takes the column pair (2 (t % 64), 2 (t % 64) + 1) and the 32-row block t / 64.
 // ---------------------------------------------------------------------------------------------
 constexpr int kColTile = 128;
 
 __global__ void __launch_bounds__(256) quant_cols_kernel(QuantArgs a) {
-  __shared__ __align__(16) uint16_t tile[kColTile][kColTile];
+  __shared__ __align__(16) uint32_t tile[kColTile][kColTile / 2];   // bf16 pairs
   const int64_t R = a.rows, C = a.cols;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColTile;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kColTile;
   const int tid = threadIdx.x;
-  // load 128 x 128 bf16: 2048 chunks of 16 B, 16 per row
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < 8; ++k) {                   // 2048 chunks of 16 B, 16 per tile row
     const int chunk = tid + 256 * k;
-    const int row = chunk >> 4, cc = (chunk & 15) << 3;
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * C + c0 + cc));
+    const int row = chunk >> 4, cc = (chunk & 15) << 2;   // cc in 32-bit words
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * C + c0) + (chunk & 15));
     *reinterpret_cast<uint4 *>(&tile[row][cc]) = v;
   }
   __syncthreads();
-  const int c = tid & 127;
-  const int half = tid >> 7;                    // rows [64*half, 64*half + 64)
-  const int64_t line = c0 + c;
-  bool zero_line = false;
-  if (a.zero_cols) zero_line = (a.zero_cols[line >> 5] >> (line & 31)) & 1u;
-  uint32_t codes_out[8];
-  uint32_t bytes_out[2];
+  const int cp = tid & 63;                        // column pair
+  const int rb = tid >> 6;                        // 32-row block inside the tile
+  float x0[32], x1[32];
 #pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    const int rb = 64 * half + 32 * b;          // first row of this block inside the tile
-    uint32_t zr = 0;
-    if (a.zero_rows) zr = a.zero_rows[(r0 + rb) >> 5];
-    float x[32];
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t w = tile[32 * rb + i][cp];
+    x0[i] = bf16_bits_to_f32(w & 0xFFFFu);
+    x1[i] = bf16_bits_to_f32(w >> 16);
+  }
+  const int64_t line0 = c0 + 2 * cp;
+  uint32_t zr = 0, zc = 0;
+  if (a.zero_rows) zr = a.zero_rows[(r0 + 32 * rb) >> 5];
+  if (a.zero_cols) zc = (a.zero_cols[line0 >> 5] >> (line0 & 31)) & 3u;
+  if (zr | zc) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float v = bf16_bits_to_f32(tile[rb + i][c]);
-      x[i] = (zero_line || ((zr >> i) & 1u)) ? 0.0f : v;
-    }
-    if (a.hadamard) {
-      butterfly_stage<32, 1>(x);
-      butterfly_stage<32, 2>(x);
-      butterfly_stage<32, 4>(x);
-      butterfly_stage<32, 8>(x);
-      butterfly_stage<32, 16>(x);
-      const float cst = inv_sqrt32();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], cst);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    const uint32_t byte = mx_scale_byte(amax);
-    bytes_out[b] = byte;
-    const float inv_s = mx_inv_scale(byte);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t word = 0;
-      if (amax > 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) word |= e2m1_code(x[8 * w + i], inv_s) << (4 * i);
-      }
-      codes_out[4 * b + w] = word;
+      const bool zrow = (zr >> i) & 1u;
+      if (zrow || (zc & 1u)) x0[i] = 0.0f;
+      if (zrow || (zc & 2u)) x1[i] = 0.0f;
     }
   }
-  uint4 *dst = reinterpret_cast<uint4 *>(a.codes + line * (R >> 1) + ((r0 + 64 * half) >> 1));
-  dst[0] = make_uint4(codes_out[0], codes_out[1], codes_out[2], codes_out[3]);
-  dst[1] = make_uint4(codes_out[4], codes_out[5], codes_out[6], codes_out[7]);
-  const int64_t blk = (r0 + 64 * half) >> 5;    // even
-  const int64_t off = a.scale_layout == 0 ? line * (R >> 5) + blk : tiled_sf_offset(line, blk, R);
-  *reinterpret_cast<uint16_t *>(a.scales + off) =
-      static_cast<uint16_t>(bytes_out[0] | (bytes_out[1] << 8));
+  if (a.hadamard) {
+    fwht32(x0);
+    fwht32(x1);
+  }
+  const int64_t blk = (r0 >> 5) + rb;
+  uint4 codes;
+  uint32_t byte = quantize_block(x0, codes);
+  *reinterpret_cast<uint4 *>(a.codes + line0 * (R >> 1) + (blk << 4)) = codes;
+  a.scales[scale_offset(a.scale_layout, line0, blk, R)] = static_cast<uint8_t>(byte);
+  byte = quantize_block(x1, codes);
+  *reinterpret_cast<uint4 *>(a.codes + (line0 + 1) * (R >> 1) + (blk << 4)) = codes;
+  a.scales[scale_offset(a.scale_layout, line0 + 1, blk, R)] = static_cast<uint8_t>(byte);
 }
 
 }  // namespace
 
 cudaError_t launch_quant(const QuantArgs &a, int inner_axis, int num_sms, cudaStream_t s) {
   if (inner_axis == 1) {
-    const int64_t total = a.rows * (a.cols >> 3);
+    const int64_t total = a.rows * (a.cols >> 5);
     int64_t blocks = (total + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8 * 2;   // ~2 waves of 8 CTAs/SM
-    if (blocks > 2 * cap) blocks = 2 * cap;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
     quant_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
   } else {
     dim3 grid(static_cast<unsigned>(a.cols / kColTile), static_cast<unsigned>(a.rows / kColTile));
