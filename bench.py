@@ -270,7 +270,10 @@ class Bench:
     # ------------------------------------------------------------------ end to end (host buffers)
     def e2e(self, steps: int, warmup: int):
         """Same metric through the C ABI with pinned host buffers: every step copies X, W, G_Y of
-        each linear host->device and Y, dX, dW device->host inside the timed region."""
+        each linear host->device and Y, dX, dW device->host inside the timed region.  Copies run
+        on their own streams and overlap the compute of other linears: linear i's upload waits
+        for the previous step's compute on its buffers, its compute waits for its upload and for
+        the previous step's download of its outputs, its download waits for its compute."""
         q = self.q
         host = []
         for c in self.cases:
@@ -280,22 +283,51 @@ class Bench:
             host.append(h)
         h2d = sum(h[k].numel() * 2 for h in host for k in ("X", "W", "GY"))
         d2h = sum(h[k].numel() * 2 for h in host for k in ("Y", "dX", "dW"))
+        s_up, s_comp, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        n = len(self.cases)
+        ev_comp = [None] * n
+        ev_down = [None] * n
 
         def one():
-            for c, h in zip(self.cases, host):
-                c.X.copy_(h["X"], non_blocking=True)
-                c.W.copy_(h["W"], non_blocking=True)
-                c.GY.copy_(h["GY"], non_blocking=True)
-                q.adahop_linear_fwd(c.plan, c.X, c.W, c.Y, self.ws)
-                q.adahop_linear_bwd(c.plan, c.GY, c.X, c.W, c.dX, c.dW, self.ws)
-                h["Y"].copy_(c.Y, non_blocking=True)
-                h["dX"].copy_(c.dX, non_blocking=True)
-                h["dW"].copy_(c.dW, non_blocking=True)
+            for i, (c, h) in enumerate(zip(self.cases, host)):
+                up = torch.cuda.Event()
+                with torch.cuda.stream(s_up):
+                    if ev_comp[i] is not None:
+                        s_up.wait_event(ev_comp[i])
+                    c.X.copy_(h["X"], non_blocking=True)
+                    c.W.copy_(h["W"], non_blocking=True)
+                    c.GY.copy_(h["GY"], non_blocking=True)
+                    up.record(s_up)
+                s_comp.wait_event(up)
+                if ev_down[i] is not None:
+                    s_comp.wait_event(ev_down[i])
+                q.adahop_linear_fwd(c.plan, c.X, c.W, c.Y, self.ws, stream=s_comp)
+                q.adahop_linear_bwd(c.plan, c.GY, c.X, c.W, c.dX, c.dW, self.ws, stream=s_comp)
+                ev_comp[i] = torch.cuda.Event()
+                ev_comp[i].record(s_comp)
+                with torch.cuda.stream(s_down):
+                    s_down.wait_event(ev_comp[i])
+                    h["Y"].copy_(c.Y, non_blocking=True)
+                    h["dX"].copy_(c.dX, non_blocking=True)
+                    h["dW"].copy_(c.dW, non_blocking=True)
+                    ev_down[i] = torch.cuda.Event()
+                    ev_down[i].record(s_down)
+
         for _ in range(warmup):
             one()
         torch.cuda.synchronize()
-        ms = cuda_time_ms(one, steps)
-        return ms, h2d, d2h
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(s_up)
+        s_comp.wait_event(start)
+        s_down.wait_event(start)
+        for _ in range(steps):
+            one()
+        s_down.wait_event(ev_comp[-1])
+        for e in ev_down:
+            s_down.wait_event(e)
+        end.record(s_down)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / steps, h2d, d2h
 
 
 # ------------------------------------------------------------------------------------ CPU oracle

@@ -81,7 +81,8 @@ adahop_status get_encoder(EncodeTiledFn *fn) {
 
 // 2D tiled map over a row-major matrix: `inner` elements per row (contiguous), `outer` rows.
 adahop_status make_map(CUtensorMap *map, CUtensorMapDataType dt, size_t elem_bytes, const void *base,
-                       uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+                       uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                       CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc;
   ST_TRY(get_encoder(&enc));
   const cuuint64_t dims[2] = {inner, outer};
@@ -89,7 +90,7 @@ adahop_status make_map(CUtensorMap *map, CUtensorMapDataType dt, size_t elem_byt
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
@@ -261,6 +262,7 @@ adahop_status mxf4_gemm(const Ctx &cx, const uint8_t *ac, const uint8_t *asf, co
                         const void *Bo, int r, void *C, int out_dtype) {
   GemmMaps maps;
   std::memset(&maps, 0, sizeof(maps));
+  // 128-byte rows (256 E2M1 codes, or 64 bf16 outlier columns) with the 128-byte swizzle
   ST_TRY(make_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ac, J / 2, P, 128, 128));
   ST_TRY(make_map(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, bc, J / 2, Q, 128, 256));
   if (r > 0) {

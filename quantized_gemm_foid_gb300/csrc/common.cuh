@@ -62,14 +62,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Returns false if the wait ran out
-// (kWaitLimitNs) or *abort became non-zero meanwhile; never spins forever.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          const volatile int *abort) {
+// (kWaitLimitNs) or *abort became non-zero meanwhile; never spins forever.  sleep_ns > 0 backs
+// off between polls so that a warp waiting a long time does not take issue slots from the warps
+// sharing its SM sub-partition (latency-critical waits pass 0).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                          uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
+    if (sleep_ns) __nanosleep(sleep_ns);
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 63u) == 0) {
       if (abort && *abort) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }

@@ -64,5 +64,6 @@ struct GemmMaps {
 };
 cudaError_t launch_gemm(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s);
 size_t gemm_smem_bytes(int kind);
+int gemm_tail_cols_per_stage();
 
 }  // namespace adahop

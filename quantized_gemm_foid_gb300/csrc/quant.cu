@@ -21,7 +21,7 @@
 //                stages in registers, one 16-byte code store (a warp stores 512 contiguous bytes).
 //   cols kernel: J = rows (the transposed orientation).  A 128 x 128 tile is staged in shared
 //                memory; each thread reads a column pair as 32-bit words and transforms one
-//                32-row block of both columns in registers.
+//                32-row block of each of the two columns in turn, in registers.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantArgs a) {
 // ---------------------------------------------------------------------------------------------
 constexpr int kColTile = 128;
 
-__global__ void __launch_bounds__(256) quant_cols_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(256, 3) quant_cols_kernel(QuantArgs a) {
   __shared__ __align__(16) uint32_t tile[kColTile][kColTile / 2];   // bf16 pairs
   const int64_t R = a.rows, C = a.cols;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColTile;
@@ -190,37 +190,31 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantArgs a) {
   __syncthreads();
   const int cp = tid & 63;                        // column pair
   const int rb = tid >> 6;                        // 32-row block inside the tile
-  float x0[32], x1[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint32_t w = tile[32 * rb + i][cp];
-    x0[i] = bf16_bits_to_f32(w & 0xFFFFu);
-    x1[i] = bf16_bits_to_f32(w >> 16);
-  }
-  const int64_t line0 = c0 + 2 * cp;
-  uint32_t zr = 0, zc = 0;
+  const int64_t blk = (r0 >> 5) + rb;
+  uint32_t zr = 0;
   if (a.zero_rows) zr = a.zero_rows[(r0 + 32 * rb) >> 5];
-  if (a.zero_cols) zc = (a.zero_cols[line0 >> 5] >> (line0 & 31)) & 3u;
-  if (zr | zc) {
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {                   // the two columns of the pair, one at a time
+    const int64_t line = c0 + 2 * cp + h;
+    uint32_t zmask = zr;
+    if (a.zero_cols && ((a.zero_cols[line >> 5] >> (line & 31)) & 1u)) zmask = 0xFFFFFFFFu;
+    float x[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const bool zrow = (zr >> i) & 1u;
-      if (zrow || (zc & 1u)) x0[i] = 0.0f;
-      if (zrow || (zc & 2u)) x1[i] = 0.0f;
+      const uint32_t w = tile[32 * rb + i][cp];
+      x[i] = bf16_bits_to_f32(h ? (w >> 16) : (w & 0xFFFFu));
     }
+    if (zmask) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if ((zmask >> i) & 1u) x[i] = 0.0f;
+    }
+    if (a.hadamard) fwht32(x);
+    uint4 codes;
+    const uint32_t byte = quantize_block(x, codes);
+    *reinterpret_cast<uint4 *>(a.codes + line * (R >> 1) + (blk << 4)) = codes;
+    a.scales[scale_offset(a.scale_layout, line, blk, R)] = static_cast<uint8_t>(byte);
   }
-  if (a.hadamard) {
-    fwht32(x0);
-    fwht32(x1);
-  }
-  const int64_t blk = (r0 >> 5) + rb;
-  uint4 codes;
-  uint32_t byte = quantize_block(x0, codes);
-  *reinterpret_cast<uint4 *>(a.codes + line0 * (R >> 1) + (blk << 4)) = codes;
-  a.scales[scale_offset(a.scale_layout, line0, blk, R)] = static_cast<uint8_t>(byte);
-  byte = quantize_block(x1, codes);
-  *reinterpret_cast<uint4 *>(a.codes + (line0 + 1) * (R >> 1) + (blk << 4)) = codes;
-  a.scales[scale_offset(a.scale_layout, line0 + 1, blk, R)] = static_cast<uint8_t>(byte);
 }
 
 }  // namespace
