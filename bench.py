@@ -211,6 +211,31 @@ class Bench:
                 "uniform_over_linears": all((c.plan.fwd, c.plan.dgrad, c.plan.wgrad) == (p.fwd, p.dgrad, p.wgrad)
                                             for c in self.cases)}
 
+    # ------------------------------------------------------------------ Table 3 variants
+    def variants(self, steps: int = 5):
+        """The same step under the plans of the pages' Table 3 rows, on the same kernels: all-BF16
+        (the cuBLAS-free tcgen05 BF16 GEMM for all three GEMMs), plain MXFP4 (no Hadamard, no
+        OE), uniform MXFP4 + Hadamard (IHT on every GEMM) and AdaHOP (the calibrated plan)."""
+        q = self.q
+        saved = [(c.plan.fwd, c.plan.dgrad, c.plan.wgrad) for c in self.cases]
+        out = {}
+        try:
+            for name, strat in (("bf16", 3), ("mxfp4", 4), ("mxfp4_had", 0), ("adahop", None)):
+                for c, orig in zip(self.cases, saved):
+                    c.plan.fwd, c.plan.dgrad, c.plan.wgrad = orig if strat is None else (strat, strat, strat)
+                self.step()
+                torch.cuda.synchronize()
+                ms = cuda_time_ms(self.step, steps)
+                out[name] = {"ms_per_step": round(ms, 3),
+                             "eff_tflops": round(self.flops_per_step / ms / 1e9, 1)}
+        finally:
+            for c, orig in zip(self.cases, saved):
+                c.plan.fwd, c.plan.dgrad, c.plan.wgrad = orig
+        base = out["bf16"]["ms_per_step"]
+        for v in out.values():
+            v["speedup_vs_bf16"] = round(base / v["ms_per_step"], 3)
+        return out
+
     # ------------------------------------------------------------------ dominant kernel (K3)
     def gemm_roofline(self, reps: int = 3):
         """Times the fused MXFP4 (+BF16 outlier) GEMM of every GEMM of one step on its own
@@ -418,6 +443,89 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def rel_mse_rows(Y, X, W, rows) -> float:
+    """||Y - X.W^T||^2 / ||X.W^T||^2 over the sampled rows, the product taken exactly in float64."""
+    exact = X[rows].double() @ W.double().t()
+    diff = Y[rows].double() - exact
+    return float((diff * diff).sum() / (exact * exact).sum())
+
+
+def sweep(q, device, args):
+    """OE rank / batch sweep on the Llama3.1-8B down projection (K = 14336, N = 4096): forward
+    latency (CUDA events) and relative MSE against the exact product for each M and rank, for a
+    Column-wise X with `rank` outlier columns x50 under OE-Right, the same X under IHT only, and a
+    None control under OE-Right.  Prints one JSON object."""
+    from synthetic.workloads import SWEEP_M, SWEEP_RANKS, sweep_workload
+    K, N = 14336, 4096
+    points = []
+    Ms = [int(m) for m in args.sweep_m.split(",")] if args.sweep_m else list(SWEEP_M)
+    for M in Ms:
+        for r in SWEEP_RANKS:
+            for label, control, strategy in (("oe_right", False, q.OE_RIGHT), ("iht_only", False, q.IHT),
+                                             ("none_control", True, q.OE_RIGHT)):
+                if label == "iht_only" and r == 0:
+                    continue
+                wl = sweep_workload(M, r, control=control)
+                X, W, _ = tensor_recipes(wl, 0, device=device)
+                plan = q.make_plan(q.PAT_COL if not control else q.PAT_NONE, q.PAT_NONE, q.PAT_NONE,
+                                   strategy, q.IHT, q.IHT, r if strategy == q.OE_RIGHT else 0)
+                ws = q.new_workspace(q.adahop_workspace_size(plan, M, N, K), device=device)
+                Y = torch.empty((M, N), dtype=torch.float32, device=device)
+                fn = lambda: q.adahop_linear_fwd(plan, X, W, Y, ws)
+                fn()
+                ms = cuda_time_ms(fn, 5)
+                assert q.adahop_get_device_status(ws) == 0
+                g = torch.Generator(device="cpu").manual_seed(M + r)
+                rows = torch.randperm(M, generator=g)[:256].to(device)
+                points.append({"M": M, "rank": r, "case": label, "ms": round(ms, 4),
+                               "tflops": round(2 * M * N * K / ms / 1e9, 1),
+                               "rel_mse": rel_mse_rows(Y, X, W, rows)})
+                del X, W, Y, ws
+                torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "llama3.1-8b down projection, Fwd", "K": K, "N": N, "points": points}))
+
+
+def quality(q, device, args):
+    """Relative MSE of Fwd, dgrad and wgrad of the Llama3.1-8B gate projection under the Table 3
+    plans (BF16, plain MXFP4, uniform MXFP4 + Hadamard, AdaHOP), each against the exact float64
+    product on 128 sampled output rows.  Prints one JSON object."""
+    wl = WORKLOADS[WORKLOAD]
+    li = 4                                      # gate projection
+    X, W, GY = tensor_recipes(wl, li, device=device)
+    M, K = X.shape
+    N = W.shape[0]
+    cal = q.adahop_calibrate(X, W, GY, q.new_workspace(1 << 22, device=device))
+    g = torch.Generator(device="cpu").manual_seed(7)
+    rows = {"fwd": torch.randperm(M, generator=g)[:128].to(device),
+            "dgrad": torch.randperm(M, generator=g)[:128].to(device),
+            "wgrad": torch.randperm(N, generator=g)[:128].to(device)}
+    exact = {"fwd": X[rows["fwd"]].double() @ W.double().t(),
+             "dgrad": GY[rows["dgrad"]].double() @ W.double(),
+             "wgrad": GY[:, rows["wgrad"]].double().t() @ X.double()}
+    out = {}
+    for name, strat in (("bf16", 3), ("mxfp4", 4), ("mxfp4_had", 0), ("adahop", None)):
+        plan = q.make_plan(cal.x, cal.w, cal.gy, *((cal.fwd, cal.dgrad, cal.wgrad) if strat is None
+                                                   else (strat, strat, strat)), cal.oe_rank)
+        ws = q.new_workspace(q.adahop_workspace_size(plan, M, N, K), device=device)
+        Y = torch.empty((M, N), dtype=torch.float32, device=device)
+        dX = torch.empty((M, K), dtype=torch.float32, device=device)
+        dW = torch.empty((N, K), dtype=torch.float32, device=device)
+        q.adahop_linear_fwd(plan, X, W, Y, ws)
+        q.adahop_linear_bwd(plan, GY, X, W, dX, dW, ws)
+        assert q.adahop_get_device_status(ws) == 0
+        res = {}
+        for gemm, C in (("fwd", Y), ("dgrad", dX), ("wgrad", dW)):
+            d = C[rows[gemm]].double() - exact[gemm]
+            res[gemm] = float((d * d).sum() / (exact[gemm] * exact[gemm]).sum())
+        out[name] = res
+        del ws, Y, dX, dW
+    from quantized_gemm_foid_gb300.binding import STRATEGY_NAMES
+    print(json.dumps({"quality": "llama3.1-8b gate projection (M=32768, N=14336, K=4096), rel-MSE vs exact",
+                      "adahop_plan": {"fwd": STRATEGY_NAMES[cal.fwd], "dgrad": STRATEGY_NAMES[cal.dgrad],
+                                      "wgrad": STRATEGY_NAMES[cal.wgrad], "rank": cal.oe_rank},
+                      "rel_mse": out}))
+
+
 def profile(q, device, args):
     """Workloads for the committed ncu summaries (profiles/); no timing, no bench line."""
     if args.profile == "step":
@@ -454,6 +562,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["adahop", "reference"], default="adahop")
+    ap.add_argument("--sweep", action="store_true",
+                    help="OE rank / batch sweep (latency and relative MSE); prints one JSON object")
+    ap.add_argument("--sweep-m", default=None, help="comma-separated M values for --sweep")
+    ap.add_argument("--quality", action="store_true",
+                    help="relative MSE of the Table 3 plans on the 8B gate projection; prints one JSON object")
     ap.add_argument("--profile", choices=["step", "gemm"], default=None,
                     help="for ncu only (prints no bench line): 'step' = warm-up steps then one step "
                          "of the workload; 'gemm' = three launches of the fused MXFP4 GEMM on the "
@@ -471,6 +584,12 @@ def main():
     import quantized_gemm_foid_gb300 as q
     if args.profile:
         profile(q, device, args)
+        return
+    if args.sweep:
+        sweep(q, device, args)
+        return
+    if args.quality:
+        quality(q, device, args)
         return
 
     peaks, peak_kind = load_peaks()
@@ -493,6 +612,7 @@ def main():
     ms = max_over_ranks(world, ms)
     gflops, gsec, per_gemm = b.gemm_roofline()
     prep = b.prep_bandwidth()
+    variants = b.variants()
     clocks = sampler.stop()
     st = q.adahop_get_device_status(b.ws)
     if st != 0:
@@ -518,6 +638,7 @@ def main():
                      "traffic": None, "launches": len(per_gemm)},
         "prep": {"kernel": "IHT + MXFP4 quantiser", "bound": "hbm", "peak_gbs": peaks.get("hbm_gbs"),
                  **{k: dict(v, frac=round(v["gbs"] / peaks.get("hbm_gbs", 6800.0), 3)) for k, v in prep.items()}},
+        "variants": variants,
         "gemms": per_gemm,
         "clocks": clocks,
         "e2e": {"value": b.flops_per_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
