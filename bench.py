@@ -201,6 +201,16 @@ class Bench:
             shared = (p.dgrad in (1, 2) and p.wgrad in (1, 2) and p.oe_rank > 0 and
                       oe_source("dgrad", p.dgrad, pats) == oe_source("wgrad", p.wgrad, pats))
             n += launches_per_gemm("wgrad", p.wgrad, p.oe_rank, pats, shared)
+            # prep fusion: one dual-orientation pass replaces the two quantisations of G_Y when
+            # both GEMMs quantise it with the same Hadamard setting and outlier mask
+            def gy_mask(gemm, st):
+                if st in (1, 2) and p.oe_rank > 0:
+                    t, axis = oe_source(gemm, st, pats)
+                    return axis if t == "GY" else -1
+                return -1
+            if (p.dgrad != 3 and p.wgrad != 3 and (p.dgrad == 4) == (p.wgrad == 4)
+                    and gy_mask("dgrad", p.dgrad) == gy_mask("wgrad", p.wgrad)):
+                n -= 1
         return n
 
     def strategies(self) -> dict:

@@ -182,6 +182,18 @@ adahop_status adahop_quantize_mxfp4(const void *T, int64_t rows, int64_t cols, i
                                     const uint32_t *zero_cols_mask, uint8_t *codes,
                                     uint8_t *scales, int scale_layout, adahop_stream_t stream);
 
+/* Both orientations of adahop_quantize_mxfp4 from one read of T (prep fusion): codes_rows /
+ * scales_rows receive exactly what inner_axis 1 produces (lines = rows, J = cols), codes_cols /
+ * scales_cols exactly what inner_axis 0 produces (lines = cols, J = rows), with the same masks,
+ * Hadamard flag and scale layout.  adahop_linear_bwd uses it for G_Y when dgrad and wgrad need
+ * the same residual.  Traffic 2 + 2 x 0.53 bytes per element instead of 2 x 2.53. */
+adahop_status adahop_quantize_mxfp4_dual(const void *T, int64_t rows, int64_t cols, int hadamard,
+                                         const uint32_t *zero_rows_mask,
+                                         const uint32_t *zero_cols_mask, uint8_t *codes_rows,
+                                         uint8_t *scales_rows, uint8_t *codes_cols,
+                                         uint8_t *scales_cols, int scale_layout,
+                                         adahop_stream_t stream);
+
 /* Outlier slice gather for the BF16 path.  T: rows x cols bf16; idx: int32[r] (device).
  * mode 0: out[i, :] = T[idx[i], :]          (r x cols)
  * mode 1: out[p, i] = T[p, idx[i]]          (rows x r)

@@ -49,6 +49,8 @@ PROTOTYPES = {
                                     c_void_p]),
     "adahop_quantize_mxfp4": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p,
                                       c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
+    "adahop_quantize_mxfp4_dual": (c_int, [c_void_p, c_int64, c_int64, c_int, c_void_p, c_void_p,
+                                           c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "adahop_gather": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_int, c_int, c_void_p,
                               c_void_p]),
     "adahop_gemm_mxfp4": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64,

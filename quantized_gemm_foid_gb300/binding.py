@@ -166,6 +166,15 @@ def adahop_quantize_mxfp4(T, inner_axis: int, hadamard: int, zero_rows_mask, zer
                                      _stream(stream)), "adahop_quantize_mxfp4")
 
 
+def adahop_quantize_mxfp4_dual(T, hadamard: int, zero_rows_mask, zero_cols_mask, codes_rows, scales_rows,
+                               codes_cols, scales_cols, scale_layout: int = 0, stream=None) -> None:
+    _cuda(T, "T", torch.bfloat16)
+    rows, cols = T.shape
+    _check(LIB.adahop_quantize_mxfp4_dual(_p(T), rows, cols, hadamard, _p(zero_rows_mask), _p(zero_cols_mask),
+                                          _p(codes_rows), _p(scales_rows), _p(codes_cols), _p(scales_cols),
+                                          scale_layout, _stream(stream)), "adahop_quantize_mxfp4_dual")
+
+
 def adahop_gather(T, idx, r: int, mode: int, out, stream=None) -> None:
     _cuda(T, "T", torch.bfloat16)
     rows, cols = T.shape

@@ -291,8 +291,14 @@ struct FoidCache {
   int tensor = -1, axis = -1, r = -1;
 };
 
+// A operand already quantised (codes + tensor-core scales) by the dual-orientation pass.
+struct PreA {
+  uint8_t *codes, *sf;
+};
+
 adahop_status run_gemm(const Ctx &cx, int gemm, int strategy, int r, const Tensor t[3],
-                       const int pats[3], void *C, int out_dtype, FoidCache *fc) {
+                       const int pats[3], void *C, int out_dtype, FoidCache *fc,
+                       const PreA *pre_a = nullptr) {
   const GemmShape sh = shape_of(gemm, t[T_X].rows, t[T_W].rows, t[T_X].cols);
   const GemmRoles ro = roles_of(gemm);
   const Tensor &ta = t[ro.a_src];
@@ -318,15 +324,20 @@ adahop_status run_gemm(const Ctx &cx, int gemm, int strategy, int r, const Tenso
     }
   }
   // quantise A (stored tensor ta, orientation a_inner_axis) and B^T (tb, b_inner_axis)
-  uint8_t *ac = ws + cx.lay.a_codes, *asf = ws + cx.lay.a_sf;
+  uint8_t *ac = pre_a ? pre_a->codes : ws + cx.lay.a_codes;
+  uint8_t *asf = pre_a ? pre_a->sf : ws + cx.lay.a_sf;
   uint8_t *bc = ws + cx.lay.b_codes, *bsf = ws + cx.lay.b_sf;
   {
     QuantArgs q{};
-    q.T = ta.p; q.rows = ta.rows; q.cols = ta.cols;
-    q.zero_rows = (oe.tensor == ro.a_src && oe.axis == 0) ? mask : nullptr;
-    q.zero_cols = (oe.tensor == ro.a_src && oe.axis == 1) ? mask : nullptr;
-    q.codes = ac; q.scales = asf; q.hadamard = hadamard; q.scale_layout = 1;
-    CUDA_TRY(launch_quant(q, ro.a_inner_axis, cx.num_sms, cx.s), "quantise A");
+    q.hadamard = hadamard;
+    q.scale_layout = 1;
+    if (!pre_a) {
+      q.T = ta.p; q.rows = ta.rows; q.cols = ta.cols;
+      q.zero_rows = (oe.tensor == ro.a_src && oe.axis == 0) ? mask : nullptr;
+      q.zero_cols = (oe.tensor == ro.a_src && oe.axis == 1) ? mask : nullptr;
+      q.codes = ac; q.scales = asf;
+      CUDA_TRY(launch_quant(q, ro.a_inner_axis, cx.num_sms, cx.s), "quantise A");
+    }
     q.T = tb.p; q.rows = tb.rows; q.cols = tb.cols;
     q.zero_rows = (oe.tensor == ro.b_src && oe.axis == 0) ? mask : nullptr;
     q.zero_cols = (oe.tensor == ro.b_src && oe.axis == 1) ? mask : nullptr;
@@ -382,6 +393,15 @@ adahop_status check_shapes(int64_t M, int64_t N, int64_t K) {
   return ADAHOP_OK;
 }
 
+// Region for G_Y's second orientation written by the dual-orientation pass of a backward call:
+// it follows the larger of the dgrad / wgrad layouts.
+size_t bwd_alt_offset(int64_t M, int64_t N, int64_t K, int r) {
+  const int64_t lines = std::max(std::max(M, N), K);
+  const GemmShape shd = shape_of(1, M, N, K), shw = shape_of(2, M, N, K);
+  return align256(std::max(gemm_ws(shd.P, shd.Q, shd.J, r, kSizingSms, lines).total,
+                           gemm_ws(shw.P, shw.Q, shw.J, r, kSizingSms, lines).total));
+}
+
 size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
   size_t b = 0;
   const int64_t lines = std::max(std::max(M, N), K);
@@ -389,6 +409,8 @@ size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
     const GemmShape sh = shape_of(g, M, N, K);
     b = std::max(b, gemm_ws(sh.P, sh.Q, sh.J, r, kSizingSms, lines).total);
   }
+  b = std::max(b, bwd_alt_offset(M, N, K, r) + align256(static_cast<size_t>(M * N / 2)) +
+                      align256(static_cast<size_t>(M * N / 32)));
   // calibration statistics: rows + cols floats of the largest tensor
   b = std::max(b, align256(256 + sizeof(float) * static_cast<size_t>(std::max(M, N) + std::max(N, K)) + 256));
   return b;
@@ -551,13 +573,48 @@ adahop_status adahop_linear_bwd(const adahop_plan *plan, const void *GY, const v
   const GemmWs lw = gemm_ws(shw.P, shw.Q, shw.J, plan->oe_rank, kSizingSms, lines);
   FoidCache fc;
   const bool share = ld.idx == lw.idx && ld.mask == lw.mask;
+  // Prep fusion: when both GEMMs quantise G_Y (dgrad along N, wgrad along M) with the same
+  // Hadamard setting and the same outlier mask, one pass over G_Y writes both orientations.
+  PreA pre_d{}, pre_w{};
+  bool dual = false;
+  if (dX && dW && share) {
+    const int sd = plan->dgrad, sw = plan->wgrad, r = plan->oe_rank;
+    const bool quant_d = sd != ADAHOP_BF16, quant_w = sw != ADAHOP_BF16;
+    const OeChoice od = (r > 0 && (sd == ADAHOP_OE_LEFT || sd == ADAHOP_OE_RIGHT)) ? oe_choice(1, sd, pats) : OeChoice{};
+    const OeChoice ow = (r > 0 && (sw == ADAHOP_OE_LEFT || sw == ADAHOP_OE_RIGHT)) ? oe_choice(2, sw, pats) : OeChoice{};
+    const int gmask_d = od.tensor == T_GY ? od.axis : -1, gmask_w = ow.tensor == T_GY ? ow.axis : -1;
+    dual = quant_d && quant_w && ((sd == ADAHOP_MXFP4) == (sw == ADAHOP_MXFP4)) && gmask_d == gmask_w;
+    if (dual) {
+      uint8_t *ws = static_cast<uint8_t *>(workspace);
+      uint32_t *mask = reinterpret_cast<uint32_t *>(ws + ld.mask);
+      if (gmask_d >= 0) {
+        CUDA_TRY(launch_foid(t[T_GY].p, M, N, gmask_d, r, reinterpret_cast<int32_t *>(ws + ld.idx), mask,
+                             ws + ld.foid, s),
+                 "foid");
+        fc = FoidCache{T_GY, gmask_d, r};
+      }
+      const size_t alt = bwd_alt_offset(M, N, K, r);
+      pre_d = PreA{ws + ld.a_codes, ws + ld.a_sf};
+      pre_w = PreA{ws + alt, ws + alt + align256(static_cast<size_t>(M * N / 2))};
+      QuantArgs q{};
+      q.T = t[T_GY].p; q.rows = M; q.cols = N;
+      q.zero_rows = gmask_d == 0 ? mask : nullptr;
+      q.zero_cols = gmask_d == 1 ? mask : nullptr;
+      q.codes = pre_d.codes; q.scales = pre_d.sf;
+      q.hadamard = sd != ADAHOP_MXFP4;
+      q.scale_layout = 1;
+      CUDA_TRY(launch_quant_dual(q, pre_w.codes, pre_w.sf, s), "quantise G_Y (both orientations)");
+    }
+  }
   if (dX) {
     Ctx cx{s, static_cast<uint8_t *>(workspace), ld, di.num_sms};
-    ST_TRY(run_gemm(cx, 1, plan->dgrad, plan->oe_rank, t, pats, dX, out_dtype, share ? &fc : nullptr));
+    ST_TRY(run_gemm(cx, 1, plan->dgrad, plan->oe_rank, t, pats, dX, out_dtype, share ? &fc : nullptr,
+                    dual ? &pre_d : nullptr));
   }
   if (dW) {
     Ctx cx{s, static_cast<uint8_t *>(workspace), lw, di.num_sms};
-    ST_TRY(run_gemm(cx, 2, plan->wgrad, plan->oe_rank, t, pats, dW, out_dtype, share ? &fc : nullptr));
+    ST_TRY(run_gemm(cx, 2, plan->wgrad, plan->oe_rank, t, pats, dW, out_dtype, share ? &fc : nullptr,
+                    dual ? &pre_w : nullptr));
   }
   return ADAHOP_OK;
 }
@@ -628,6 +685,28 @@ adahop_status adahop_quantize_mxfp4(const void *T, int64_t rows, int64_t cols, i
   q.zero_rows = zero_rows_mask; q.zero_cols = zero_cols_mask;
   q.codes = codes; q.scales = scales; q.hadamard = hadamard; q.scale_layout = scale_layout;
   CUDA_TRY(launch_quant(q, inner_axis, di.num_sms, reinterpret_cast<cudaStream_t>(stream)), "quantise");
+  return ADAHOP_OK;
+}
+
+adahop_status adahop_quantize_mxfp4_dual(const void *T, int64_t rows, int64_t cols, int hadamard,
+                                         const uint32_t *zero_rows_mask, const uint32_t *zero_cols_mask,
+                                         uint8_t *codes_rows, uint8_t *scales_rows, uint8_t *codes_cols,
+                                         uint8_t *scales_cols, int scale_layout, adahop_stream_t stream) {
+  if (!T || !codes_rows || !scales_rows || !codes_cols || !scales_cols || (hadamard != 0 && hadamard != 1) ||
+      (scale_layout != 0 && scale_layout != 1))
+    return ADAHOP_ERR_INVALID_ARG;
+  if (!dim_ok(rows) || !dim_ok(cols)) return ADAHOP_ERR_SHAPE;
+  if (!aligned(T, 16) || !aligned(codes_rows, 16) || !aligned(scales_rows, 16) || !aligned(codes_cols, 16) ||
+      !aligned(scales_cols, 16))
+    return ADAHOP_ERR_ALIGN;
+  DeviceInfo di;
+  ST_TRY(device_info(&di));
+  QuantArgs q{};
+  q.T = static_cast<const uint16_t *>(T);
+  q.rows = rows; q.cols = cols;
+  q.zero_rows = zero_rows_mask; q.zero_cols = zero_cols_mask;
+  q.codes = codes_rows; q.scales = scales_rows; q.hadamard = hadamard; q.scale_layout = scale_layout;
+  CUDA_TRY(launch_quant_dual(q, codes_cols, scales_cols, reinterpret_cast<cudaStream_t>(stream)), "quantise (dual)");
   return ADAHOP_OK;
 }
 

@@ -26,6 +26,9 @@ struct QuantArgs {
   int scale_layout;             // 0 canonical, 1 tensor-core atoms
 };
 cudaError_t launch_quant(const QuantArgs &a, int inner_axis, int num_sms, cudaStream_t s);
+// Both orientations in one pass: a.codes / a.scales receive the J = cols orientation (lines = rows),
+// codes_cols / scales_cols the J = rows orientation (lines = cols); same masks and Hadamard flag.
+cudaError_t launch_quant_dual(const QuantArgs &a, uint8_t *codes_cols, uint8_t *scales_cols, cudaStream_t s);
 
 // FOID: stage 1 (per 2048-line chunk top-r) + stage 2 (merge, ascending indices, bitmap).
 size_t foid_scratch_bytes(int64_t lines, int r);

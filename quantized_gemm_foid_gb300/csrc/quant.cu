@@ -217,7 +217,101 @@ __global__ void __launch_bounds__(256, 3) quant_cols_kernel(QuantArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// dual kernel: both orientations of one tensor from a single read (prep fusion).  Tile 128 x 128
+// staged in shared memory with 4-word row padding (conflict-free row reads and column-pair
+// reads); each thread quantises two 32-blocks along the tile's rows (J = cols) and one 32-row
+// block of each column of a column pair (J = rows).  Same arithmetic as the two kernels above.
+// ---------------------------------------------------------------------------------------------
+constexpr int kDualPitch = kColTile / 2 + 4;     // 32-bit words per staged row
+
+__global__ void __launch_bounds__(256, 3) quant_dual_kernel(QuantArgs a, uint8_t *codes_c, uint8_t *scales_c) {
+  __shared__ __align__(16) uint32_t tile[kColTile][kDualPitch];
+  const int64_t R = a.rows, C = a.cols;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColTile;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kColTile;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int chunk = tid + 256 * k;
+    const int row = chunk >> 4, cc = (chunk & 15) << 2;
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * C + c0) + (chunk & 15));
+    *reinterpret_cast<uint4 *>(&tile[row][cc]) = v;
+  }
+  __syncthreads();
+  // (1) along the rows: row tid / 2, blocks 2 (tid % 2) and 2 (tid % 2) + 1 of the tile
+  {
+    const int rr = tid >> 1;
+    const int64_t row = r0 + rr;
+    const bool zrow = a.zero_rows && ((a.zero_rows[row >> 5] >> (row & 31)) & 1u);
+#pragma unroll 1
+    for (int b = 0; b < 2; ++b) {
+      const int bl = 2 * (tid & 1) + b;                // 32-column block inside the tile
+      const int64_t blk = (c0 >> 5) + bl;
+      uint32_t zmask = zrow ? 0xFFFFFFFFu : 0u;
+      if (a.zero_cols) zmask |= a.zero_cols[blk];
+      float x[32];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&tile[rr][16 * bl + 4 * w]);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x[8 * w + 2 * j] = bf16_bits_to_f32(u[j] & 0xFFFFu);
+          x[8 * w + 2 * j + 1] = bf16_bits_to_f32(u[j] >> 16);
+        }
+      }
+      if (zmask) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if ((zmask >> i) & 1u) x[i] = 0.0f;
+      }
+      if (a.hadamard) fwht32(x);
+      uint4 codes;
+      const uint32_t byte = quantize_block(x, codes);
+      *reinterpret_cast<uint4 *>(a.codes + row * (C >> 1) + (blk << 4)) = codes;
+      a.scales[scale_offset(a.scale_layout, row, blk, C)] = static_cast<uint8_t>(byte);
+    }
+  }
+  // (2) along the columns: column pair tid % 64, 32-row block tid / 64
+  {
+    const int cp = tid & 63;
+    const int rb = tid >> 6;
+    const int64_t blk = (r0 >> 5) + rb;
+    uint32_t zr = 0;
+    if (a.zero_rows) zr = a.zero_rows[(r0 + 32 * rb) >> 5];
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      const int64_t line = c0 + 2 * cp + h;
+      uint32_t zmask = zr;
+      if (a.zero_cols && ((a.zero_cols[line >> 5] >> (line & 31)) & 1u)) zmask = 0xFFFFFFFFu;
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t w = tile[32 * rb + i][cp];
+        x[i] = bf16_bits_to_f32(h ? (w >> 16) : (w & 0xFFFFu));
+      }
+      if (zmask) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if ((zmask >> i) & 1u) x[i] = 0.0f;
+      }
+      if (a.hadamard) fwht32(x);
+      uint4 codes;
+      const uint32_t byte = quantize_block(x, codes);
+      *reinterpret_cast<uint4 *>(codes_c + line * (R >> 1) + (blk << 4)) = codes;
+      scales_c[scale_offset(a.scale_layout, line, blk, R)] = static_cast<uint8_t>(byte);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quant_dual(const QuantArgs &a, uint8_t *codes_cols, uint8_t *scales_cols, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(a.cols / kColTile), static_cast<unsigned>(a.rows / kColTile));
+  quant_dual_kernel<<<grid, 256, 0, s>>>(a, codes_cols, scales_cols);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant(const QuantArgs &a, int inner_axis, int num_sms, cudaStream_t s) {
   if (inner_axis == 1) {

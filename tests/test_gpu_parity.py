@@ -66,6 +66,35 @@ def test_quantize_bitexact(q, shape, hadamard, inner_axis):
         assert np.array_equal(from_tiled(to_host_u8(tiled), lines, J), want_scales)
 
 
+@pytest.mark.parametrize("shape", [(128, 128), (384, 256), (256, 640)])
+@pytest.mark.parametrize("hadamard", [1, 0])
+def test_quantize_dual_bitexact(q, shape, hadamard):
+    """One pass, both orientations: each equals the oracle's quantisation of that orientation."""
+    T = _bits(shape, 12, axis="row", count=6, scale=40.0)
+    rows, cols = shape
+    dT = dev_bf16_from_bits(T)
+    for zero_rows, zero_cols in ((None, None), ([1, 33, rows - 1], None), (None, [0, 95, cols - 1])):
+        mr = to_dev(bitmap(rows, zero_rows)) if zero_rows else None
+        mc = to_dev(bitmap(cols, zero_cols)) if zero_cols else None
+        for layout in (0, 1):
+            cr = torch.zeros(rows * cols // 2, dtype=torch.uint8, device="cuda")
+            sr = torch.zeros(rows * cols // 32, dtype=torch.uint8, device="cuda")
+            cc = torch.zeros_like(cr)
+            sc = torch.zeros_like(sr)
+            q.adahop_quantize_mxfp4_dual(dT, hadamard, mr, mc, cr, sr, cc, sc, layout)
+            torch.cuda.synchronize()
+            wcr, wsr = O.quantize_operand(T, bool(hadamard), zero_rows=zero_rows, zero_cols=zero_cols)
+            wcc, wsc = O.quantize_operand(np.ascontiguousarray(T.T), bool(hadamard), zero_rows=zero_cols,
+                                          zero_cols=zero_rows)
+            assert np.array_equal(to_host_u8(cr).reshape(rows, cols // 2), wcr)
+            assert np.array_equal(to_host_u8(cc).reshape(cols, rows // 2), wcc)
+            got_sr, got_sc = to_host_u8(sr), to_host_u8(sc)
+            if layout == 1:
+                got_sr, got_sc = from_tiled(got_sr, rows, cols), from_tiled(got_sc, cols, rows)
+            assert np.array_equal(got_sr.reshape(rows, -1), wsr)
+            assert np.array_equal(got_sc.reshape(cols, -1), wsc)
+
+
 def test_quantize_edge_values(q):
     """All-zero blocks, tiny (subnormal-scale) blocks, exact ties and huge values."""
     rows, cols = 128, 256
