@@ -10,9 +10,12 @@
 // Ranking key = (float bits of var) << 32 | (0xFFFFFFFF - l): larger variance first, and for
 // equal variance the lower index first.  Keys are unique, so the top-r set is well defined.
 //
-// Stage 1 (grid): each CTA scores 2048 lines (512 threads x 4), sorts their keys in shared
-// memory (bitonic) and writes its best r.  Stage 2 (one CTA): sorts the candidates, keeps the
-// best r, writes their indices in ascending order and the bitmap of selected lines.
+// Stage 1 (grid): each CTA scores one chunk of 256..2048 lines (the smallest chunk that keeps
+// at most 8192 candidates overall), sorts their keys in shared memory (bitonic) and writes its
+// best r.  Stage 2 (one CTA): reduces the sorted runs pairwise -- the element-wise maximum of a
+// run and the reverse of its partner is a bitonic sequence holding exactly their best keys, which
+// half-cleaner steps sort again -- then writes the best r indices in ascending order and the
+// bitmap of selected lines.
 #include <mutex>
 
 #include "common.cuh"
@@ -23,8 +26,25 @@ namespace adahop {
 namespace {
 
 constexpr int kFoidThreads = 512;
-constexpr int kFoidChunk = 2048;            // lines per stage-1 CTA
-constexpr int kFoidMergeMaxKeys = 8192;     // stage-2 shared-memory capacity (64 KB)
+constexpr int kFoidMaxChunk = 2048;         // lines per stage-1 CTA, at most
+constexpr int kFoidMinChunk = 256;
+constexpr int kFoidMergeMaxKeys = 8192;     // candidates written by stage 1, at most
+constexpr int kFoidMergeSmemKeys = 16384;   // stage-2 shared memory (runs padded to a power of 2)
+
+int pow2_at_least(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+// Smallest chunk (many stage-1 CTAs) that keeps the candidate count within the merge's capacity.
+int foid_chunk(int64_t lines, int r) {
+  const int rr = r > 0 ? r : 1;
+  for (int chunk = kFoidMinChunk; chunk < kFoidMaxChunk; chunk <<= 1) {
+    if (chunk >= pow2_at_least(rr) && (lines + chunk - 1) / chunk * rr <= kFoidMergeMaxKeys) return chunk;
+  }
+  return kFoidMaxChunk;
+}
 
 __device__ __forceinline__ float bf(uint32_t b) { return __uint_as_float(b << 16); }
 
@@ -97,92 +117,132 @@ __device__ void bitonic_sort_desc(uint64_t *keys, int n) {
 template <int AXIS>
 __global__ void __launch_bounds__(kFoidThreads) foid_local_kernel(const uint16_t *__restrict__ T,
                                                                   int64_t rows, int64_t cols, int r,
-                                                                  uint64_t *cand) {
-  __shared__ uint64_t keys[kFoidChunk];
+                                                                  int chunk, uint64_t *cand) {
+  __shared__ uint64_t keys[kFoidMaxChunk];
   const int64_t lines = AXIS == 0 ? rows : cols;
-  const int64_t base = static_cast<int64_t>(blockIdx.x) * kFoidChunk;
-  for (int j = 0; j < kFoidChunk / kFoidThreads; ++j) {
-    const int local = threadIdx.x + j * kFoidThreads;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * chunk;
+  for (int local = threadIdx.x; local < chunk; local += blockDim.x) {
     const int64_t line = base + local;
     keys[local] = line < lines ? foid_key<AXIS>(T, cols, line) : 0ull;
   }
   __syncthreads();
-  bitonic_sort_desc(keys, kFoidChunk);
-  for (int i = threadIdx.x; i < r; i += blockDim.x)
-    cand[static_cast<int64_t>(blockIdx.x) * r + i] = keys[i];
+  bitonic_sort_desc(keys, chunk);
+  for (int i = threadIdx.x; i < r; i += blockDim.x) cand[static_cast<int64_t>(blockIdx.x) * r + i] = keys[i];
 }
 
-__global__ void __launch_bounds__(1024) foid_merge_kernel(const uint64_t *cand, int ncand, int np2,
-                                                          int r, int64_t lines, int32_t *idx_out,
-                                                          uint32_t *mask_out) {
+// ncand = runs * r candidates (each run sorted descending); runs are padded to rp2 in shared memory.
+__global__ void __launch_bounds__(1024) foid_merge_kernel(const uint64_t *cand, int runs, int r, int rp2,
+                                                          int64_t lines, int32_t *idx_out, uint32_t *mask_out) {
   extern __shared__ uint64_t skeys[];
   __shared__ uint32_t sidx[256];
-  for (int i = threadIdx.x; i < np2; i += blockDim.x) skeys[i] = i < ncand ? cand[i] : 0ull;
+  const int n = runs * rp2;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int run = i / rp2, k = i - run * rp2;
+    skeys[i] = k < r ? cand[static_cast<int64_t>(run) * r + k] : 0ull;
+  }
   const int64_t words = (lines + 31) >> 5;
   if (mask_out) {
     for (int64_t w = threadIdx.x; w < words; w += blockDim.x) mask_out[w] = 0u;
   }
   __syncthreads();
-  if (r > 0) {
-    bitonic_sort_desc(skeys, np2);
-    // the best r lines, then ascending order (r <= 256; pad with 0xFFFFFFFF)
-    int rp2 = 1;
-    while (rp2 < r) rp2 <<= 1;
-    for (int i = threadIdx.x; i < rp2; i += blockDim.x)
-      sidx[i] = i < r ? 0xFFFFFFFFu - static_cast<uint32_t>(skeys[i] & 0xFFFFFFFFull) : 0xFFFFFFFFu;
+  if (r == 0) return;
+  int g = runs;
+  while (g > 1) {
+    const int pairs = g >> 1;
+    const int m = pairs * rp2;
+    // max(run 2p, reverse(run 2p+1)) -> run p, staged through registers (at most 16 per thread)
+    uint64_t tmp[kFoidMergeSmemKeys / 1024];
+    int cnt = 0;
+    for (int i = threadIdx.x; i < m; i += blockDim.x, ++cnt) {
+      const int pr = i / rp2, k = i - pr * rp2;
+      const uint64_t a = skeys[(2 * pr) * rp2 + k], b = skeys[(2 * pr + 1) * rp2 + (rp2 - 1 - k)];
+      tmp[cnt] = a > b ? a : b;
+    }
+    uint64_t odd[kFoidMergeSmemKeys / 1024];
+    int ocnt = 0;
+    if (g & 1) {
+      for (int k = threadIdx.x; k < rp2; k += blockDim.x, ++ocnt) odd[ocnt] = skeys[(g - 1) * rp2 + k];
+    }
     __syncthreads();
-    for (int k = 2; k <= rp2; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = threadIdx.x; i < rp2; i += blockDim.x) {
-          const int ixj = i ^ j;
-          if (ixj > i) {
-            const uint32_t a = sidx[i], b = sidx[ixj];
-            const bool up = (i & k) == 0;   // ascending run
-            if (up ? (a > b) : (a < b)) {
-              sidx[i] = b;
-              sidx[ixj] = a;
-            }
+    cnt = 0;
+    for (int i = threadIdx.x; i < m; i += blockDim.x, ++cnt) skeys[i] = tmp[cnt];
+    ocnt = 0;
+    if (g & 1) {
+      for (int k = threadIdx.x; k < rp2; k += blockDim.x, ++ocnt) skeys[pairs * rp2 + k] = odd[ocnt];
+    }
+    __syncthreads();
+    // each merged run is bitonic: half-cleaner steps sort it descending
+    for (int j = rp2 >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < m; i += blockDim.x) {
+        if ((i & j) == 0) {
+          const uint64_t a = skeys[i], b = skeys[i + j];
+          if (a < b) {
+            skeys[i] = b;
+            skeys[i + j] = a;
           }
         }
-        __syncthreads();
       }
+      __syncthreads();
     }
-    for (int i = threadIdx.x; i < r; i += blockDim.x) {
-      const uint32_t l = sidx[i];
-      idx_out[i] = static_cast<int32_t>(l);
-      if (mask_out) atomicOr(mask_out + (l >> 5), 1u << (l & 31));
+    g = pairs + (g & 1);
+  }
+  // the best r lines, then ascending order (pad with 0xFFFFFFFF)
+  for (int i = threadIdx.x; i < rp2; i += blockDim.x)
+    sidx[i] = i < r ? 0xFFFFFFFFu - static_cast<uint32_t>(skeys[i] & 0xFFFFFFFFull) : 0xFFFFFFFFu;
+  __syncthreads();
+  for (int k = 2; k <= rp2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < rp2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint32_t a = sidx[i], b = sidx[ixj];
+          const bool up = (i & k) == 0;   // ascending run
+          if (up ? (a > b) : (a < b)) {
+            sidx[i] = b;
+            sidx[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
     }
+  }
+  for (int i = threadIdx.x; i < r; i += blockDim.x) {
+    const uint32_t l = sidx[i];
+    idx_out[i] = static_cast<int32_t>(l);
+    if (mask_out) atomicOr(mask_out + (l >> 5), 1u << (l & 31));
   }
 }
 
 }  // namespace
 
 size_t foid_scratch_bytes(int64_t lines, int r) {
-  const int64_t chunks = (lines + kFoidChunk - 1) / kFoidChunk;
+  const int chunk = foid_chunk(lines, r);
+  const int64_t chunks = (lines + chunk - 1) / chunk;
   return static_cast<size_t>(chunks * (r > 0 ? r : 1)) * sizeof(uint64_t);
 }
 
 cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
                         int32_t *idx_out, uint32_t *mask_out, void *scratch, cudaStream_t s) {
   const int64_t lines = axis == 0 ? rows : cols;
-  const int64_t chunks = (lines + kFoidChunk - 1) / kFoidChunk;
-  const int64_t ncand = chunks * r;
-  if (ncand > kFoidMergeMaxKeys || r > 256) return cudaErrorInvalidValue;
+  if (r < 0 || r > 256) return cudaErrorInvalidValue;
+  const int chunk = foid_chunk(lines, r);
+  const int64_t chunks = (lines + chunk - 1) / chunk;
+  if (chunks * r > kFoidMergeMaxKeys) return cudaErrorInvalidValue;
+  const int rp2 = pow2_at_least(r > 0 ? r : 1);
   uint64_t *cand = static_cast<uint64_t *>(scratch);
   if (r > 0) {
+    const int threads = chunk < kFoidThreads ? chunk : kFoidThreads;
     if (axis == 0)
-      foid_local_kernel<0><<<static_cast<unsigned>(chunks), kFoidThreads, 0, s>>>(T, rows, cols, r, cand);
+      foid_local_kernel<0><<<static_cast<unsigned>(chunks), threads, 0, s>>>(T, rows, cols, r, chunk, cand);
     else
-      foid_local_kernel<1><<<static_cast<unsigned>(chunks), kFoidThreads, 0, s>>>(T, rows, cols, r, cand);
+      foid_local_kernel<1><<<static_cast<unsigned>(chunks), threads, 0, s>>>(T, rows, cols, r, chunk, cand);
   }
-  int np2 = 1;
-  while (np2 < ncand) np2 <<= 1;
-  const size_t smem = static_cast<size_t>(np2) * sizeof(uint64_t);
+  const int runs = r > 0 ? static_cast<int>(chunks) : 0;
+  const size_t smem = static_cast<size_t>(runs > 0 ? runs * rp2 : 1) * sizeof(uint64_t);
   cudaError_t e = cudaFuncSetAttribute(foid_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kFoidMergeMaxKeys * static_cast<int>(sizeof(uint64_t)));
+                                       kFoidMergeSmemKeys * static_cast<int>(sizeof(uint64_t)));
   if (e != cudaSuccess) return e;
-  foid_merge_kernel<<<1, 1024, smem, s>>>(cand, static_cast<int>(ncand), np2, r, lines, idx_out,
-                                          mask_out);
+  foid_merge_kernel<<<1, 1024, smem, s>>>(cand, runs, r, rp2, lines, idx_out, mask_out);
   return cudaGetLastError();
 }
 
