@@ -262,12 +262,18 @@ adahop_status mxf4_gemm(const Ctx &cx, const uint8_t *ac, const uint8_t *asf, co
                         const void *Bo, int r, void *C, int out_dtype) {
   GemmMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  // 128-byte rows (256 E2M1 codes, or 64 bf16 outlier columns) with the 128-byte swizzle
+  // 128-byte rows (256 E2M1 codes, or 64 bf16 outlier columns) with the 128-byte swizzle; each
+  // CTA of a pair loads 128 rows of A and 128 rows of B
   ST_TRY(make_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ac, J / 2, P, 128, 128));
-  ST_TRY(make_map(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, bc, J / 2, Q, 128, 256));
+  ST_TRY(make_map(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, bc, J / 2, Q, 128, 128));
+  // scale atoms (512 bytes = 128 uint32 each), two consecutive atoms per load
+  ST_TRY(make_map(&maps.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, asf, 128, (P / 128) * (J / 128), 128, 2,
+                  CU_TENSOR_MAP_SWIZZLE_NONE));
+  ST_TRY(make_map(&maps.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, bsf, 128, (Q / 128) * (J / 128), 128, 2,
+                  CU_TENSOR_MAP_SWIZZLE_NONE));
   if (r > 0) {
     ST_TRY(make_map(&maps.ao, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ao, r, P, 64, 128));
-    ST_TRY(make_map(&maps.bo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Bo, r, Q, 64, 256));
+    ST_TRY(make_map(&maps.bo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Bo, r, Q, 64, 128));
   } else {
     maps.ao = maps.a;
     maps.bo = maps.b;

@@ -1,27 +1,35 @@
-// K3 / K5 / K6: persistent tcgen05 GEMM for sm_103a.
+// K3 / K5 / K6: persistent tcgen05 GEMMs for sm_103a.
 //
 // AdaHOP appendix implementation notes, "Fused MXFP4+BF16 GEMM": the MXFP4 residual product and
 // the BF16 outlier product are computed together (on CDNA4 with 64 x 64 tiles).  Here both are
-// tcgen05 MMAs that accumulate into the SAME float32 tile in tensor memory:
-//   kind 0 (MXFP4): for each 256-wide slice of J, four kind::mxf4.block_scale MMAs
-//                   (128 x 256 x 64, E2M1 operands in shared memory, UE8M0 scale factors copied
-//                   to tensor memory with tcgen05.cp), then ceil(r/64) stages of kind::f16 MMAs
-//                   over the BF16 outlier slices A_o (P x r) and B_o (Q x r):
-//                   C = deq(A) deq(B)^T + A_o B_o^T.
-//                   Operand rows are 128 bytes (128-byte swizzle), 4 stages of 51 KB (a variant
-//                   with 64-byte rows and 8 stages of 26 KB measured 11% slower).
-//   kind 1 (BF16):  kind::f16 MMAs (128 x 256 x 16) over bf16 operands stored J-contiguous
-//                   ("K-major") or MN-contiguous ("MN-major"); 128-byte rows (128-byte swizzle),
-//                   4 stages of 48 KB; optional split-K into float32 partials (the outlier GEMM
-//                   of outer OE, which has only r rows).
+// tcgen05 MMAs that accumulate into the SAME float32 tile in tensor memory.
 //
-// Warp roles (320 threads): warp 0 = TMA producer (one elected lane), warp 1 = tensor-memory
-// allocator + MMA issuer (one lane), warps 2..9 = epilogue (two warps per 32-lane quadrant, each
-// draining 128 of the 256 accumulator columns).  Tensor memory holds the 128 x 256 float32
-// accumulator (columns 0..255) and per-stage scale factors (columns 256..351).
-// The epilogue copies the accumulator to registers and releases it before storing, so the next
-// tile's MMAs overlap the stores.  Every wait is bounded (common.cuh); on expiry the kernel sets
-// the status word, stops issuing work, drains what it issued, frees tensor memory and returns.
+// kind 0 (MXFP4, K3) runs on CTA pairs (clusters of two CTAs on paired SMs, cta_group::2): a pair
+// owns a 256 x 256 tile of C; each CTA holds its 128 rows of A and its 128-row half of B in
+// shared memory, and one thread of the even CTA issues 256 x 256 x 64 kind::mxf4.block_scale
+// MMAs that read both CTAs' operands and accumulate into both CTAs' tensor memory (each CTA keeps
+// its own 128 x 256 float32 rows).  Per SM that is half the B bytes per FLOP of a single-CTA
+// 128 x 256 tile.  For each 256-wide slice of J: four MXFP4 MMAs (UE8M0 scale factors copied to
+// tensor memory with tcgen05.cp: each CTA supplies its own 128 rows of A scales and all 256 rows
+// of B scales), then ceil(r/64) stages of kind::f16 MMAs over the BF16 outlier slices A_o (P x r)
+// and B_o (Q x r): C = deq(A) deq(B)^T + A_o B_o^T.  Operand rows are 128 bytes (128-byte
+// swizzle); 6 stages of 35 KB per CTA.  Every TMA load of either CTA is counted on the even CTA's
+// stage barrier, the MMA commits release the stage in both CTAs, and the odd CTA's epilogue warps
+// release the accumulator on the even CTA's barrier.
+//
+// kind 1 (BF16, K5 / K6) runs on single CTAs: kind::f16 MMAs (128 x 256 x 16) over bf16
+// operands stored J-contiguous ("K-major") or MN-contiguous ("MN-major"); 128-byte rows
+// (128-byte swizzle), 4 stages of 48 KB; optional split-K into float32 partials (the outlier GEMM
+// of outer OE, which has only r rows).
+//
+// Warp roles (320 threads per CTA): warp 0 = TMA producer (one lane), warp 1 = tensor-memory
+// allocator + MMA issuer (one lane; in a pair only the even CTA's issues), warps 2..9 =
+// epilogue (two warps per 32-lane quadrant, each draining 128 of the 256 accumulator columns).
+// Tensor memory holds the 128 x 256 float32 accumulator (columns 0..255) and per-stage scale
+// factors above it.  The epilogue copies the accumulator to registers and releases it before
+// storing, so the next tile's MMAs overlap the stores.  Every mbarrier wait is bounded
+// (common.cuh); on expiry the kernel sets the status word, stops issuing work, drains what it
+// issued, frees tensor memory and returns.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -29,50 +37,44 @@ namespace adahop {
 
 namespace {
 
-constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;              // scale factors live above the accumulator
-constexpr uint32_t kLayoutSw64 = 4;
 
-template <int KIND>
-struct Cfg;
-template <>
-struct Cfg<0> {                                    // MXFP4 (+ BF16 tail)
-  static constexpr int kStages = 4;
+// ------------------------------------------------------------------ kind 0: MXFP4 on CTA pairs
+struct PairCfg {
+  static constexpr int kBM = 256;                  // rows of C per pair (128 per CTA)
+  static constexpr int kStages = 6;
   static constexpr int kBK = 256;                  // J elements per main-loop stage
-  static constexpr uint32_t kRowBytes = 128;
-  static constexpr uint32_t kABytes = BM * 128;    // 16 KB
-  static constexpr uint32_t kBBytes = BN * 128;    // 32 KB
-  static constexpr uint32_t kSFA = kABytes + kBBytes;      // 2 atoms (128 rows x 8 blocks)
-  static constexpr uint32_t kSFB = kSFA + 1024;            // 4 atoms (256 rows x 8 blocks)
-  static constexpr uint32_t kStageBytes = kSFB + 2048;     // 51 KB
-  static constexpr uint32_t kLayout = kLayoutSw128;
-  static constexpr uint32_t kSBO = 8 * 128;                // 8-row swizzle atom
+  static constexpr uint32_t kABytes = 128 * 128;   // this CTA's 128 rows x 128 bytes of codes
+  static constexpr uint32_t kBBytes = 128 * 128;   // this CTA's 128 of the 256 B rows
+  static constexpr uint32_t kSFA = kABytes + kBBytes;      // 2 atoms: this CTA's 128 rows x 8 blocks
+  static constexpr uint32_t kSFB = kSFA + 1024;            // 4 atoms: all 256 B rows x 8 blocks
+  static constexpr uint32_t kStageBytes = kSFB + 2048;     // 35 KB
   static constexpr uint32_t kSfCols = 24;                  // TMEM columns of scale factors per stage
+  // bytes counted on the even CTA's stage barrier: both CTAs' loads (TMA counts whole boxes)
+  static constexpr uint32_t kTxMain = 2 * kStageBytes;
+  static constexpr uint32_t kTxTail = 2 * (kABytes + kBBytes);
 };
-template <>
-struct Cfg<1> {                                    // BF16
+static_assert(PairCfg::kStageBytes % 1024 == 0, "stage layout");
+static_assert(kSfTmemBase + PairCfg::kStages * PairCfg::kSfCols <= kTmemCols, "TMEM budget");
+
+// ------------------------------------------------------------------ kind 1: BF16 on single CTAs
+struct Bf16Cfg {
+  static constexpr int kBM = 128;
   static constexpr int kStages = 4;
   static constexpr int kBK = 64;
-  static constexpr uint32_t kRowBytes = 128;
-  static constexpr uint32_t kABytes = BM * 128;    // 16 KB
+  static constexpr uint32_t kABytes = 128 * 128;   // 16 KB
   static constexpr uint32_t kBBytes = BN * 128;    // 32 KB
-  static constexpr uint32_t kSFA = 0, kSFB = 0;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kLayout = kLayoutSw128;
-  static constexpr uint32_t kSBO = 8 * 128;
-  static constexpr uint32_t kSfCols = 0;
 };
-static_assert(Cfg<0>::kStageBytes % 1024 == 0, "stage layout");
-static_assert(kSfTmemBase + Cfg<0>::kStages * Cfg<0>::kSfCols <= kTmemCols, "TMEM budget");
 
-template <int KIND>
+template <int STAGES>
 struct SmemCtl {
-  uint64_t full[Cfg<KIND>::kStages];
-  uint64_t empty[Cfg<KIND>::kStages];
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
@@ -87,7 +89,7 @@ struct TileInfo {
 };
 
 __device__ __forceinline__ TileInfo tile_info(const GemmArgs &g, int64_t tile, int64_t tiles_m,
-                                              int64_t tiles_n, int num_k, bool n_fastest) {
+                                              int64_t tiles_n, int num_k, bool n_fastest, int bm) {
   TileInfo t;
   const int64_t mn = tiles_m * tiles_n;
   t.split = static_cast<int>(tile / mn);
@@ -100,7 +102,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &g, int64_t tile, i
     ni = rem / tiles_m;
     mi = rem - ni * tiles_m;
   }
-  t.m0 = mi * BM;
+  t.m0 = mi * bm;
   t.n0 = ni * BN;
   if (g.splits > 1) {
     const int per = (num_k + g.splits - 1) / g.splits;
@@ -113,22 +115,308 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &g, int64_t tile, i
   return t;
 }
 
-template <int KIND>
+// Stores 32 accumulator columns (col .. col+31, clipped at Q) of one row of C, or of the split's
+// float32 partials.
+__device__ __forceinline__ void store_row32(const GemmArgs &g, bool to_partial, int split, int64_t row,
+                                            int64_t col, const uint32_t (&v)[32]) {
+  const bool full = col + 32 <= g.Q;
+  if (to_partial || g.out_dtype == 1) {
+    float *dst = (to_partial ? g.c_partial + static_cast<int64_t>(split) * g.P * g.Q
+                             : static_cast<float *>(g.C)) +
+                 row * g.Q + col;
+    if (full) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4 *>(dst)[q] =
+            make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (col + e < g.Q) dst[e] = __uint_as_float(v[e]);
+    }
+  } else {
+    uint16_t *dst = static_cast<uint16_t *>(g.C) + row * g.Q + col;
+    if (full) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = f32_to_bf16_bits(__uint_as_float(v[8 * q + 2 * e])) |
+                 (f32_to_bf16_bits(__uint_as_float(v[8 * q + 2 * e + 1])) << 16);
+        reinterpret_cast<uint4 *>(dst)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (col + e < g.Q) dst[e] = static_cast<uint16_t>(f32_to_bf16_bits(__uint_as_float(v[e])));
+    }
+  }
+}
+
+// =============================================================================================
+// kind 0: MXFP4 (+ BF16 outlier tail), CTA pairs
+// =============================================================================================
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
-  using C = Cfg<KIND>;
-  constexpr bool mxf4 = KIND == 0;
+    gemm_mxf4_pair_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
+  using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ SmemCtl<KIND> ctl;
+  __shared__ SmemCtl<C::kStages> ctl;
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // same offset in both CTAs
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();           // 0: issues the MMAs; 1: its peer
+  const uint32_t peer = rank ^ 1u;
+  const int64_t pair = blockIdx.x >> 1;
+  const int64_t num_pairs = gridDim.x >> 1;
+  const int num_k = static_cast<int>((g.J + C::kBK - 1) / C::kBK);
+  const int tail = g.tail_stages;
+  const int64_t tiles_m = (g.P + C::kBM - 1) / C::kBM;
+  const int64_t tiles_n = (g.Q + BN - 1) / BN;
+  const int64_t num_tiles = tiles_m * tiles_n;
+  const bool n_fastest = g.P >= g.Q;                 // stream the larger operand once
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&ctl.full[s]), 1);          // the even CTA's producer + both CTAs' bytes
+      mbar_init(smem_u32(&ctl.empty[s]), 1);         // one multicast MMA commit
+    }
+    mbar_init(smem_u32(&ctl.acc_full), 1);
+    mbar_init(smem_u32(&ctl.acc_empty), 2 * kEpiWarps);   // epilogue warps of both CTAs
+    mbar_init(smem_u32(&ctl.drain), 1);
+    ctl.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();                                // barriers of both CTAs initialised
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int *abort_flag = &ctl.abort_flag;
+  const uint32_t peer_abort = cluster_map(smem_u32(&ctl.abort_flag), peer);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    // The whole warp runs the loop (warp-uniform operands; every lane waits on the barriers and
+    // the warp agrees on each outcome); one elected lane issues.
+    if (elect_one()) {
+      prefetch_tensormap(&maps.a);
+      prefetch_tensormap(&maps.b);
+      prefetch_tensormap(&maps.sfa);
+      prefetch_tensormap(&maps.sfb);
+      if (tail) {
+        prefetch_tensormap(&maps.ao);
+        prefetch_tensormap(&maps.bo);
+      }
+    }
+    __syncwarp();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    const int32_t atoms_per_rowblk = static_cast<int32_t>(g.J >> 7);   // 4-block scale atoms along J
+    const int64_t nblocks = (g.Q + 127) >> 7;
+    for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+      const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
+      const int32_t my_m0 = static_cast<int32_t>(t.m0 + 128 * rank);
+      const int32_t my_n0 = static_cast<int32_t>(t.n0 + 128 * rank);
+      const int32_t mb = my_m0 >> 7;
+      const int32_t nb0 = static_cast<int32_t>(t.n0 >> 7);
+      const int32_t nb1 = (nb0 + 1 < nblocks) ? nb0 + 1 : nb0;   // ragged Q: reuse finite scales
+      const int nsteps = num_k + tail;
+      for (int step = 0; step < nsteps; ++step) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, 32))) {
+          ok = false;
+          break;
+        }
+        const uint32_t sA = smem_base + stage * C::kStageBytes;
+        const uint32_t sB = sA + C::kABytes;
+        const uint32_t full_own = smem_u32(&ctl.full[stage]);
+        const uint32_t full = cluster_map(full_own, 0);          // the even CTA's barrier
+        if (elect_one()) {
+          if (step < num_k) {
+            if (rank == 0) mbar_arrive_expect_tx(full_own, C::kTxMain);
+            tma_load_2d_pair(sA, &maps.a, full, step * 128, my_m0);
+            tma_load_2d_pair(sB, &maps.b, full, step * 128, my_n0);
+            // scale atoms: two per 128 rows per stage (the second is unused when the last slice
+            // of a J that is an odd multiple of 128 is half full; rows past P read zeros)
+            tma_load_2d_pair(sA + C::kSFA, &maps.sfa, full, 0, mb * atoms_per_rowblk + 2 * step);
+            tma_load_2d_pair(sA + C::kSFB, &maps.sfb, full, 0, nb0 * atoms_per_rowblk + 2 * step);
+            tma_load_2d_pair(sA + C::kSFB + 1024, &maps.sfb, full, 0, nb1 * atoms_per_rowblk + 2 * step);
+          } else {
+            // BF16 outlier tail: 64 of the r outlier columns (128 bytes) per stage
+            const int32_t r0 = (step - num_k) * 64;
+            if (rank == 0) mbar_arrive_expect_tx(full_own, C::kTxTail);
+            tma_load_2d_pair(sA, &maps.ao, full, r0, my_m0);
+            tma_load_2d_pair(sB, &maps.bo, full, r0, my_n0);
+          }
+        }
+        __syncwarp();
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // a CTA that gives up tells its peer too, so that neither waits out the full limit
+      *abort_flag = 1;
+      st_cluster_u32(peer_abort, 1u);
+      report_status(g.status, kStatusTimeout);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (even CTA)
+    // The whole warp runs the loop; one elected lane issues the copies, MMAs and commits.
+    if (rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      constexpr uint32_t idesc_bf16 = make_idesc_bf16(C::kBM, BN, false, false);
+      for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        const int nsteps = num_k + tail;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.acc_empty), acc_phase ^ 1u, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int step = 0; step < nsteps; ++step) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_base + stage * C::kStageBytes;
+          const uint32_t sB = sA + C::kABytes;
+          if (elect_one()) {
+            if (step < num_k) {
+              const uint32_t sfa_t = tmem + kSfTmemBase + stage * C::kSfCols;
+              const uint32_t sfb_t = sfa_t + 8;
+              // the last slice of a J that is an odd multiple of 128 holds one scale atom and
+              // two MMAs
+              const bool half = (step == num_k - 1) && ((g.J & 255) != 0);
+#pragma unroll
+              for (int ka = 0; ka < 2; ++ka) {
+                if (ka == 1 && half) break;
+                // SF-A atom ka -> columns sfa + 4 ka; SF-B rows 0..127 -> sfb + 8 ka, 128..255 -> +4
+                tmem_cp_32x128b_x4_pair(sfa_t + 4 * ka,
+                                        make_smem_desc(sA + C::kSFA + 512 * ka, 0, 128, kLayoutNone));
+                tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka,
+                                        make_smem_desc(sA + C::kSFB + 512 * ka, 0, 128, kLayoutNone));
+                tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka + 4,
+                                        make_smem_desc(sA + C::kSFB + 1024 + 512 * ka, 0, 128, kLayoutNone));
+              }
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                if (kk == 2 && half) break;
+                const uint64_t adesc = make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
+                const uint64_t bdesc = make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
+                constexpr uint32_t idesc0 = make_idesc_mxf4(C::kBM, BN, 0, 0);
+                constexpr uint32_t idesc2 = make_idesc_mxf4(C::kBM, BN, 2, 2);
+                mma_mxf4_pair(tmem, adesc, bdesc, (kk & 1) ? idesc2 : idesc0, sfa_t + 4 * (kk >> 1),
+                              sfb_t + 8 * (kk >> 1), (step > 0 || kk > 0) ? 1u : 0u);
+              }
+            } else {
+              // BF16 outlier tail: four K=16 MMAs over 128-byte rows (never the first step)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t adesc = make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
+                const uint64_t bdesc = make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
+                mma_bf16_pair(tmem, adesc, bdesc, idesc_bf16, 1u);
+              }
+            }
+            tc_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);   // frees the stage in both CTAs
+          }
+          __syncwarp();
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (elect_one()) tc_commit_pair(smem_u32(&ctl.acc_full), 0x3);   // both accumulators ready
+        __syncwarp();
+        acc_phase ^= 1u;
+      }
+      if (!ok && lane == 0) {
+        *abort_flag = 1;
+        st_cluster_u32(peer_abort, 1u);
+        report_status(g.status, kStatusTimeout);
+      }
+      // drain: wait (bounded) until every MMA / copy this warp issued has completed
+      if (elect_one()) tc_commit_pair(smem_u32(&ctl.drain), 0x1);
+      __syncwarp();
+      if (!mbar_wait(smem_u32(&ctl.drain), 0, nullptr) && lane == 0) report_status(g.status, kStatusTimeout);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int quad = warp & 3;                        // TMEM lanes 32*quad .. 32*quad+31
+    const int half = (warp - 2) >> 2;                 // accumulator columns 128*half ..
+    const uint32_t acc_empty = cluster_map(smem_u32(&ctl.acc_empty), 0);
+    const bool can_store = g.C != nullptr;
+    if (!can_store && threadIdx.x == 64) report_status(g.status, kStatusBadArg);
+    uint32_t acc_phase = 0;
+    for (int64_t tile = pair; tile < num_tiles; tile += num_pairs) {
+      const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
+      bool ready = true;
+      if (lane == 0) ready = mbar_wait(smem_u32(&ctl.acc_full), acc_phase, abort_flag, 128);
+      ready = __shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0) != 0;
+      if (!ready) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          st_cluster_u32(peer_abort, 1u);
+          report_status(g.status, kStatusTimeout);
+        }
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[4][32];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * quad) << 16) + 128u * half;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + 32u * j, v[j]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty);
+      acc_phase ^= 1u;
+
+      const int64_t row = t.m0 + 128 * rank + 32 * quad + lane;
+      if (can_store && row < g.P) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t col = t.n0 + 128 * half + 32 * j;
+          if (col < g.Q) store_row32(g, false, 0, row, col, v[j]);
+        }
+      }
+    }
+  }
+
+  // neither CTA frees tensor memory or exits while its peer may still signal it
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
+}
+
+// =============================================================================================
+// kind 1: BF16, single CTAs
+// =============================================================================================
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
+  using C = Bf16Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ SmemCtl<C::kStages> ctl;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // swizzle atoms need alignment
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_k = static_cast<int>((g.J + C::kBK - 1) / C::kBK);
-  const int tail = mxf4 ? g.tail_stages : 0;
-  const int64_t tiles_m = (g.P + BM - 1) / BM;
+  const int64_t tiles_m = (g.P + C::kBM - 1) / C::kBM;
   const int64_t tiles_n = (g.Q + BN - 1) / BN;
   const int64_t num_tiles = tiles_m * tiles_n * (g.splits > 1 ? g.splits : 1);
-  // stream the larger operand once: n fastest keeps B resident while A is read once
   const bool n_fastest = g.P >= g.Q;
 
   if (threadIdx.x == 0) {
@@ -157,19 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&maps.a);
       prefetch_tensormap(&maps.b);
-      if (tail) {
-        prefetch_tensormap(&maps.ao);
-        prefetch_tensormap(&maps.bo);
-      }
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const int64_t atoms_per_rowblk = g.J >> 7;          // 4-block scale atoms along J
-      const int64_t nblocks = (g.Q + 127) >> 7;
       for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest);
-        const int nsteps = (t.k_end - t.k_begin) + tail;
-        for (int step = 0; step < nsteps; ++step) {
+        const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
+        for (int ks = t.k_begin; ks < t.k_end; ++ks) {
           if (!mbar_wait(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, 32)) {
             ok = false;
             break;
@@ -177,45 +458,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sA = smem_base + stage * C::kStageBytes;
           const uint32_t sB = sA + C::kABytes;
           const uint32_t full = smem_u32(&ctl.full[stage]);
-          const int ks = t.k_begin + step;
-          if (step < t.k_end - t.k_begin) {
-            if (mxf4) {
-              // 128 bytes of codes per row; two 4-block scale atoms per 128 rows (one when the
-              // last slice of a J that is an odd multiple of 128 is half full)
-              const bool half = (ks == num_k - 1) && ((g.J & 255) != 0);
-              const uint32_t sf_chunk = half ? 512u : 1024u;
-              mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes + 3 * sf_chunk);
-              tma_load_2d(sA, &maps.a, full, ks * 128, static_cast<int32_t>(t.m0));
-              tma_load_2d(sB, &maps.b, full, ks * 128, static_cast<int32_t>(t.n0));
-              const int64_t mb = t.m0 >> 7;
-              const int64_t nb0 = t.n0 >> 7;
-              const int64_t nb1 = (nb0 + 1 < nblocks) ? nb0 + 1 : nb0;   // ragged Q: reuse finite scales
-              bulk_load(sA + C::kSFA, g.sfa + (mb * atoms_per_rowblk + 2 * ks) * 512, sf_chunk, full);
-              bulk_load(sA + C::kSFB, g.sfb + (nb0 * atoms_per_rowblk + 2 * ks) * 512, sf_chunk, full);
-              bulk_load(sA + C::kSFB + 1024, g.sfb + (nb1 * atoms_per_rowblk + 2 * ks) * 512, sf_chunk, full);
-            } else {
-              mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes);
-              const int32_t k0 = ks * 64;
-              if (g.a_mn_major) {
-                tma_load_2d(sA, &maps.a, full, static_cast<int32_t>(t.m0), k0);
-                tma_load_2d(sA + 8192, &maps.a, full, static_cast<int32_t>(t.m0 + 64), k0);
-              } else {
-                tma_load_2d(sA, &maps.a, full, k0, static_cast<int32_t>(t.m0));
-              }
-              if (g.b_mn_major) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                  tma_load_2d(sB + c * 8192, &maps.b, full, static_cast<int32_t>(t.n0 + 64 * c), k0);
-              } else {
-                tma_load_2d(sB, &maps.b, full, k0, static_cast<int32_t>(t.n0));
-              }
-            }
+          mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes);
+          const int32_t k0 = ks * 64;
+          if (g.a_mn_major) {
+            tma_load_2d(sA, &maps.a, full, static_cast<int32_t>(t.m0), k0);
+            tma_load_2d(sA + 8192, &maps.a, full, static_cast<int32_t>(t.m0 + 64), k0);
           } else {
-            // BF16 outlier tail (kind 0): 64 of the r outlier columns (128 bytes) per stage
-            const int32_t r0 = (step - (t.k_end - t.k_begin)) * 64;
-            mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes);
-            tma_load_2d(sA, &maps.ao, full, r0, static_cast<int32_t>(t.m0));
-            tma_load_2d(sB, &maps.bo, full, r0, static_cast<int32_t>(t.n0));
+            tma_load_2d(sA, &maps.a, full, k0, static_cast<int32_t>(t.m0));
+          }
+          if (g.b_mn_major) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d(sB + c * 8192, &maps.b, full, static_cast<int32_t>(t.n0 + 64 * c), k0);
+          } else {
+            tma_load_2d(sB, &maps.b, full, k0, static_cast<int32_t>(t.n0));
           }
           if (++stage == C::kStages) {
             stage = 0;
@@ -235,19 +491,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      const uint32_t idesc_bf16 =
-          make_idesc_bf16(BM, BN, !mxf4 && g.a_mn_major != 0, !mxf4 && g.b_mn_major != 0);
+      const uint32_t idesc = make_idesc_bf16(C::kBM, BN, g.a_mn_major != 0, g.b_mn_major != 0);
       for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest);
-        const int nmain = t.k_end - t.k_begin;
-        const int nsteps = nmain + tail;
+        const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
         if (!mbar_wait(smem_u32(&ctl.acc_empty), acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t accumulate = 0;
-        for (int step = 0; step < nsteps; ++step) {
+        for (int ks = t.k_begin; ks < t.k_end; ++ks) {
           if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag)) {
             ok = false;
             break;
@@ -255,48 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sA = smem_base + stage * C::kStageBytes;
           const uint32_t sB = sA + C::kABytes;
-          if (mxf4 && step < nmain) {
-            const uint32_t sfa_t = tmem + kSfTmemBase + stage * C::kSfCols;
-            const uint32_t sfb_t = sfa_t + 8;
-            const int ks = t.k_begin + step;
-            const bool half = (ks == num_k - 1) && ((g.J & 255) != 0);
-            const int katoms = half ? 1 : 2;
-            for (int ka = 0; ka < katoms; ++ka) {
-              // SF-A atom ka -> columns sfa + 4 ka; SF-B rows 0..127 -> sfb + 8 ka, 128..255 -> +4
-              tmem_cp_32x128b_x4(sfa_t + 4 * ka, make_smem_desc(sA + C::kSFA + 512 * ka, 0, 128, kLayoutNone));
-              tmem_cp_32x128b_x4(sfb_t + 8 * ka, make_smem_desc(sA + C::kSFB + 512 * ka, 0, 128, kLayoutNone));
-              tmem_cp_32x128b_x4(sfb_t + 8 * ka + 4,
-                                 make_smem_desc(sA + C::kSFB + 1024 + 512 * ka, 0, 128, kLayoutNone));
-            }
-            const int kk_end = half ? 2 : 4;
-            for (int kk = 0; kk < kk_end; ++kk) {
-              const uint64_t adesc = make_smem_desc(sA + 32 * kk, 16, C::kSBO, C::kLayout);
-              const uint64_t bdesc = make_smem_desc(sB + 32 * kk, 16, C::kSBO, C::kLayout);
-              const uint32_t sf_id = static_cast<uint32_t>(kk & 1) * 2u;
-              mma_mxf4(tmem, adesc, bdesc, make_idesc_mxf4(BM, BN, sf_id, sf_id), sfa_t + 4 * (kk >> 1),
-                       sfb_t + 8 * (kk >> 1), accumulate);
-              accumulate = 1;
-            }
-          } else if (mxf4) {
-            // BF16 outlier tail: four K=16 MMAs over 128-byte rows
+          // four K=16 MMAs over 128-byte rows (K-major) or 16-row groups (MN-major)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t adesc = make_smem_desc(sA + 32 * kk, 16, C::kSBO, C::kLayout);
-              const uint64_t bdesc = make_smem_desc(sB + 32 * kk, 16, C::kSBO, C::kLayout);
-              mma_bf16(tmem, adesc, bdesc, idesc_bf16, accumulate);
-              accumulate = 1;
-            }
-          } else {
-            // BF16 main loop: four K=16 MMAs over 128-byte rows (K-major) or 16-row groups (MN-major)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t adesc = g.a_mn_major ? make_smem_desc(sA + 2048 * kk, 8192, 1024, kLayoutSw128)
-                                                  : make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
-              const uint64_t bdesc = g.b_mn_major ? make_smem_desc(sB + 2048 * kk, 8192, 1024, kLayoutSw128)
-                                                  : make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
-              mma_bf16(tmem, adesc, bdesc, idesc_bf16, accumulate);
-              accumulate = 1;
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = g.a_mn_major ? make_smem_desc(sA + 2048 * kk, 8192, 1024, kLayoutSw128)
+                                                : make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
+            const uint64_t bdesc = g.b_mn_major ? make_smem_desc(sB + 2048 * kk, 8192, 1024, kLayoutSw128)
+                                                : make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
+            mma_bf16(tmem, adesc, bdesc, idesc, accumulate);
+            accumulate = 1;
           }
           tc_commit(smem_u32(&ctl.empty[stage]));      // frees the smem stage when MMAs finish
           if (++stage == C::kStages) {
@@ -312,14 +532,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         report_status(g.status, kStatusTimeout);
       }
-      // drain: wait (bounded) until every MMA / copy this thread issued has completed
+      // drain: wait (bounded) until every MMA this thread issued has completed
       tc_commit(smem_u32(&ctl.drain));
       if (!mbar_wait(smem_u32(&ctl.drain), 0, nullptr)) report_status(g.status, kStatusTimeout);
     }
   } else {
     // ------------------------------------------------------------------ epilogue warps
-    const int quad = warp & 3;                        // TMEM lanes 32*quad .. 32*quad+31
-    const int half = (warp - 2) >> 2;                 // accumulator columns 128*half ..
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     // Partial mode (split-K or not) is chosen by a non-null c_partial; with neither output the
     // tiles are computed but nothing is stored and the status word records the bad argument.
     const bool to_partial = g.c_partial != nullptr;
@@ -327,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!can_store && threadIdx.x == 64) report_status(g.status, kStatusBadArg);
     uint32_t acc_phase = 0;
     for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest);
+      const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
       bool ready = true;
       if (lane == 0) ready = mbar_wait(smem_u32(&ctl.acc_full), acc_phase, abort_flag, 128);
       ready = __shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0) != 0;
@@ -354,42 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int64_t col = t.n0 + 128 * half + 32 * j;
-          if (col >= g.Q) continue;
-          const bool full = col + 32 <= g.Q;
-          if (to_partial || g.out_dtype == 1) {
-            float *dst = (to_partial ? g.c_partial + static_cast<int64_t>(t.split) * g.P * g.Q
-                                     : static_cast<float *>(g.C)) +
-                         row * g.Q + col;
-            if (full) {
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                reinterpret_cast<float4 *>(dst)[q] =
-                    make_float4(__uint_as_float(v[j][4 * q]), __uint_as_float(v[j][4 * q + 1]),
-                                __uint_as_float(v[j][4 * q + 2]), __uint_as_float(v[j][4 * q + 3]));
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (col + e < g.Q) dst[e] = __uint_as_float(v[j][e]);
-            }
-          } else {
-            uint16_t *dst = static_cast<uint16_t *>(g.C) + row * g.Q + col;
-            if (full) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  w[e] = f32_to_bf16_bits(__uint_as_float(v[j][8 * q + 2 * e])) |
-                         (f32_to_bf16_bits(__uint_as_float(v[j][8 * q + 2 * e + 1])) << 16);
-                reinterpret_cast<uint4 *>(dst)[q] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (col + e < g.Q)
-                  dst[e] = static_cast<uint16_t>(f32_to_bf16_bits(__uint_as_float(v[j][e])));
-            }
-          }
+          if (col < g.Q) store_row32(g, to_partial, t.split, row, col, v[j]);
         }
       }
     }
@@ -401,28 +586,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int KIND>
-cudaError_t launch_kind(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
-  const size_t smem = gemm_smem_bytes(KIND);
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+cudaLaunchConfig_t pair_launch_config(cudaLaunchAttribute *attr, unsigned grid, size_t smem, cudaStream_t s) {
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Co-resident CTA pairs of the MXFP4 kernel on the current device (its persistent grid), cached.
+int pair_capacity(int num_sms) {
+  constexpr int kMaxDevices = 64;
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return num_sms / 2;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_launch_config(attr, static_cast<unsigned>(num_sms & ~1), gemm_smem_bytes(0), 0);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf4_pair_kernel, &cfg) != cudaSuccess || clusters <= 0) {
+    (void)cudaGetLastError();
+    clusters = num_sms / 2;
+  }
+  cached[dev] = clusters;
+  return clusters;
+}
+
+cudaError_t launch_mxf4(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
+  const size_t smem = gemm_smem_bytes(0);
+  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int64_t tiles = ((g.P + BM - 1) / BM) * ((g.Q + BN - 1) / BN) * (g.splits > 1 ? g.splits : 1);
+  const int64_t tiles = ((g.P + PairCfg::kBM - 1) / PairCfg::kBM) * ((g.Q + BN - 1) / BN);
+  const int64_t cap = pair_capacity(num_sms);
+  const unsigned pairs = static_cast<unsigned>(tiles < cap ? tiles : cap);
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_launch_config(attr, 2 * pairs, smem, s);
+  e = cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, maps, g);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bf16(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
+  const size_t smem = gemm_smem_bytes(1);
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = ((g.P + Bf16Cfg::kBM - 1) / Bf16Cfg::kBM) * ((g.Q + BN - 1) / BN) *
+                        (g.splits > 1 ? g.splits : 1);
   const unsigned grid = static_cast<unsigned>(tiles < num_sms ? tiles : num_sms);
-  gemm_kernel<KIND><<<grid, kThreads, smem, s>>>(maps, g);
+  gemm_bf16_kernel<<<grid, kThreads, smem, s>>>(maps, g);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes(int kind) {
-  return kind == 0 ? Cfg<0>::kStages * Cfg<0>::kStageBytes + 1024 : Cfg<1>::kStages * Cfg<1>::kStageBytes + 1024;
+  return kind == 0 ? PairCfg::kStages * PairCfg::kStageBytes + 1024
+                   : Bf16Cfg::kStages * Bf16Cfg::kStageBytes + 1024;
 }
 
 int gemm_tail_cols_per_stage() { return 64; }
 
 cudaError_t launch_gemm(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
-  return g.kind == 0 ? launch_kind<0>(g, maps, num_sms, s) : launch_kind<1>(g, maps, num_sms, s);
+  return g.kind == 0 ? launch_mxf4(g, maps, num_sms, s) : launch_bf16(g, maps, num_sms, s);
 }
 
 }  // namespace adahop

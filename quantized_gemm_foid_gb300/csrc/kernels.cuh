@@ -54,7 +54,7 @@ struct GemmArgs {
   int64_t P, Q, J;            // C is P x Q; inner dimension J
   int kind;                   // 0 = MXFP4 (+ optional BF16 tail), 1 = BF16
   int a_mn_major, b_mn_major; // BF16 only: operand stored J-major (MN contiguous)
-  const uint8_t *sfa, *sfb;   // MXFP4 scale factors (tensor-core layout)
+  const uint8_t *sfa, *sfb;   // MXFP4 scale factors (tensor-core layout; read through maps.sfa / sfb)
   int tail_stages;            // MXFP4: ceil(r / 64) stages of BF16 outlier MMAs
   void *C;
   int out_dtype;              // 0 bf16, 1 fp32
@@ -62,8 +62,11 @@ struct GemmArgs {
   float *c_partial;           // non-null: fp32 partials (splits x P x Q) are written here, not C
   uint32_t *status;
 };
+// MXFP4: a / b are the E2M1 codes (128-byte rows, 128 rows per box), sfa / sfb the tensor-core
+// scale atoms viewed as rows of 128 uint32 (one 512-byte atom per row, two atoms per box), ao / bo
+// the BF16 outlier slices.  BF16: a / b only.
 struct GemmMaps {
-  CUtensorMap a, b, ao, bo;
+  CUtensorMap a, b, ao, bo, sfa, sfb;
 };
 cudaError_t launch_gemm(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s);
 size_t gemm_smem_bytes(int kind);
