@@ -442,22 +442,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // Whole-warp loops with one elected issuing lane keep every operand warp-uniform.
+    if (elect_one()) {
       prefetch_tensormap(&maps.a);
       prefetch_tensormap(&maps.b);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
-        for (int ks = t.k_begin; ks < t.k_end; ++ks) {
-          if (!mbar_wait(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, 32)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sA = smem_base + stage * C::kStageBytes;
-          const uint32_t sB = sA + C::kABytes;
-          const uint32_t full = smem_u32(&ctl.full[stage]);
+    }
+    __syncwarp();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
+      for (int ks = t.k_begin; ks < t.k_end; ++ks) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, 32))) {
+          ok = false;
+          break;
+        }
+        const uint32_t sA = smem_base + stage * C::kStageBytes;
+        const uint32_t sB = sA + C::kABytes;
+        const uint32_t full = smem_u32(&ctl.full[stage]);
+        if (elect_one()) {
           mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes);
           const int32_t k0 = ks * 64;
           if (g.a_mn_major) {
@@ -473,41 +477,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_2d(sB, &maps.b, full, k0, static_cast<int32_t>(t.n0));
           }
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        }
+        __syncwarp();
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      if (!ok) {
-        *abort_flag = 1;
-        report_status(g.status, kStatusTimeout);
-      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report_status(g.status, kStatusTimeout);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      const uint32_t idesc = make_idesc_bf16(C::kBM, BN, g.a_mn_major != 0, g.b_mn_major != 0);
-      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
-        if (!mbar_wait(smem_u32(&ctl.acc_empty), acc_phase ^ 1u, abort_flag)) {
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    const uint32_t idesc = make_idesc_bf16(C::kBM, BN, g.a_mn_major != 0, g.b_mn_major != 0);
+    for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.acc_empty), acc_phase ^ 1u, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int ks = t.k_begin; ks < t.k_end; ++ks) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t accumulate = 0;
-        for (int ks = t.k_begin; ks < t.k_end; ++ks) {
-          if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sA = smem_base + stage * C::kStageBytes;
-          const uint32_t sB = sA + C::kABytes;
+        const uint32_t sA = smem_base + stage * C::kStageBytes;
+        const uint32_t sB = sA + C::kABytes;
+        if (elect_one()) {
           // four K=16 MMAs over 128-byte rows (K-major) or 16-row groups (MN-major)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -515,27 +519,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 : make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
             const uint64_t bdesc = g.b_mn_major ? make_smem_desc(sB + 2048 * kk, 8192, 1024, kLayoutSw128)
                                                 : make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
-            mma_bf16(tmem, adesc, bdesc, idesc, accumulate);
-            accumulate = 1;
+            mma_bf16(tmem, adesc, bdesc, idesc, (ks > t.k_begin || kk > 0) ? 1u : 0u);
           }
           tc_commit(smem_u32(&ctl.empty[stage]));      // frees the smem stage when MMAs finish
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-        if (!ok) break;
-        tc_commit(smem_u32(&ctl.acc_full));            // accumulator ready for the epilogue
-        acc_phase ^= 1u;
+        __syncwarp();
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (!ok) {
-        *abort_flag = 1;
-        report_status(g.status, kStatusTimeout);
-      }
-      // drain: wait (bounded) until every MMA this thread issued has completed
-      tc_commit(smem_u32(&ctl.drain));
-      if (!mbar_wait(smem_u32(&ctl.drain), 0, nullptr)) report_status(g.status, kStatusTimeout);
+      if (!ok) break;
+      if (elect_one()) tc_commit(smem_u32(&ctl.acc_full));   // accumulator ready for the epilogue
+      __syncwarp();
+      acc_phase ^= 1u;
     }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report_status(g.status, kStatusTimeout);
+    }
+    // drain: wait (bounded) until every MMA this warp issued has completed
+    if (elect_one()) tc_commit(smem_u32(&ctl.drain));
+    __syncwarp();
+    if (!mbar_wait(smem_u32(&ctl.drain), 0, nullptr) && lane == 0) report_status(g.status, kStatusTimeout);
   } else {
     // ------------------------------------------------------------------ epilogue warps
     const int quad = warp & 3;
@@ -568,6 +574,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl.acc_empty));
       acc_phase ^= 1u;
+      if (t.k_end <= t.k_begin) {            // a split with no K range contributes zeros
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[j][e] = 0u;
+      }
 
       const int64_t row = t.m0 + 32 * quad + lane;
       if (can_store && row < g.P) {

@@ -218,17 +218,23 @@ def test_gemm_bf16_layouts(q, a_kmajor, b_kmajor, P, Q, J):
     assert _rel(C.cpu().numpy(), ref) <= 1e-5
 
 
-def test_gemm_bf16_split_partials(q):
-    P, Q, J, S = 64, 256, 1024, 4
+@pytest.mark.parametrize("J,S", [(1024, 4), (128, 5)])
+def test_gemm_bf16_split_partials(q, J, S):
+    # (128, 5): J holds two 64-wide K stages, so splits 1..4 have empty ranges and must hold zeros
+    P, Q = 64, 256
     A = _bits((P, J), 51)
     B = _bits((J, Q), 52)
     ref = O.bf16_to_f32(A).astype(np.float64) @ O.bf16_to_f32(B).astype(np.float64)
-    part = torch.zeros((S, P, Q), dtype=torch.float32, device="cuda")
+    part = torch.full((S, P, Q), float("nan"), dtype=torch.float32, device="cuda")
     ws = q.new_workspace(4096)
     q.adahop_gemm_bf16(dev_bf16_from_bits(A), 1, dev_bf16_from_bits(B), 0, P, Q, J, None, ws, splits=S,
                        c_partial=part)
     torch.cuda.synchronize()
     assert _rel(part.sum(0).cpu().numpy(), ref) <= 1e-5
+    per = -(-(J // 64) // S)
+    for s in range(S):
+        if s * per >= J // 64:
+            assert torch.count_nonzero(part[s]).item() == 0
 
 
 # ------------------------------------------------------------------------------ scatter-add
