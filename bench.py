@@ -134,6 +134,12 @@ class LinearCase:
         self.Y = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=device)
         self.dX = torch.empty((self.M, self.K), dtype=torch.bfloat16, device=device)
         self.dW = torch.empty((self.N, self.K), dtype=torch.bfloat16, device=device)
+        # saved context (forward -> backward), sized for plans that quantise both backward GEMMs
+        full = q.make_plan(fwd=q.IHT, dgrad=q.IHT, wgrad=q.IHT)
+        self.saved = q.new_saved(full, self.M, self.N, self.K, device=device)
+
+    def saved_bytes(self, q) -> int:
+        return q.adahop_saved_size(self.plan, self.M, self.N, self.K)
 
     def flops(self) -> int:
         return 6 * self.M * self.N * self.K
@@ -163,6 +169,14 @@ def oe_source(gemm: str, strategy: int, pats: dict):
     return (cols[0] if len(cols) == 1 else b), 1
 
 
+def zero_axis(gemm: str, strategy: int, r: int, pats: dict, tensor: str) -> int:
+    """Axis of `tensor` whose FOID lines this GEMM zeroes before quantising (-1: none)."""
+    if r <= 0 or strategy not in (1, 2):
+        return -1
+    t, axis = oe_source(gemm, strategy, pats)
+    return axis if t == tensor else -1
+
+
 def launches_per_gemm(gemm: str, strategy: int, r: int, pats: dict, foid_shared: bool) -> int:
     """Kernels the dispatcher launches for one GEMM (the launch sequence of adahop.cu)."""
     if strategy == 3:                        # BF16: one GEMM
@@ -188,8 +202,8 @@ class Bench:
     def step(self):
         q = self.q
         for c in self.cases:
-            q.adahop_linear_fwd(c.plan, c.X, c.W, c.Y, self.ws)
-            q.adahop_linear_bwd(c.plan, c.GY, c.X, c.W, c.dX, c.dW, self.ws)
+            q.adahop_linear_fwd_save(c.plan, c.X, c.W, c.Y, c.saved, self.ws)
+            q.adahop_linear_bwd_saved(c.plan, c.GY, c.X, c.W, c.saved, c.dX, c.dW, self.ws)
 
     def launches_per_step(self) -> int:
         n = 0
@@ -211,6 +225,18 @@ class Bench:
             if (p.dgrad != 3 and p.wgrad != 3 and (p.dgrad == 4) == (p.wgrad == 4)
                     and gy_mask("dgrad", p.dgrad) == gy_mask("wgrad", p.wgrad)):
                 n -= 1
+            # saved context: the backward GEMMs skip quantising X (wgrad) and W (dgrad); the forward
+            # call writes them, in its own quantisation pass when mask and Hadamard setting agree,
+            # else in a separate pass (FOID first when the backward GEMM zeroes lines)
+            r = p.oe_rank
+            for tensor, bgemm, bst in (("X", "wgrad", p.wgrad), ("W", "dgrad", p.dgrad)):
+                if bst == 3:
+                    continue
+                n -= 1
+                zf, zb = zero_axis("fwd", p.fwd, r, pats, tensor), zero_axis(bgemm, bst, r, pats, tensor)
+                dual = p.fwd != 3 and zf == zb and (p.fwd != 4) == (bst != 4)
+                if not dual:
+                    n += 1 + (2 if zb >= 0 else 0)
         return n
 
     def strategies(self) -> dict:
@@ -336,8 +362,8 @@ class Bench:
                 s_comp.wait_event(up)
                 if ev_down[i] is not None:
                     s_comp.wait_event(ev_down[i])
-                q.adahop_linear_fwd(c.plan, c.X, c.W, c.Y, self.ws, stream=s_comp)
-                q.adahop_linear_bwd(c.plan, c.GY, c.X, c.W, c.dX, c.dW, self.ws, stream=s_comp)
+                q.adahop_linear_fwd_save(c.plan, c.X, c.W, c.Y, c.saved, self.ws, stream=s_comp)
+                q.adahop_linear_bwd_saved(c.plan, c.GY, c.X, c.W, c.saved, c.dX, c.dW, self.ws, stream=s_comp)
                 ev_comp[i] = torch.cuda.Event()
                 ev_comp[i].record(s_comp)
                 with torch.cuda.stream(s_down):
@@ -654,6 +680,12 @@ def main():
         "e2e": {"value": b.flops_per_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": b.launches_per_step() * args.steps,
+        # forward -> backward context per step: X in the wgrad orientation and W in the dgrad
+        # orientation (MXFP4 codes + scales) against the bf16 copies of X a BF16 backward keeps
+        "saved_context": {"bytes_per_step": sum(c.saved_bytes(q) for c in b.cases),
+                          "bf16_x_bytes_per_step": sum(2 * c.M * c.K for c in b.cases),
+                          "x_compression": round(2 / (0.5 + 1 / 32), 3),
+                          "note": "X itself is still read in bf16 for the r outlier lines of inner OE"},
     }
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline()

@@ -124,6 +124,39 @@ adahop_status adahop_linear_bwd(const adahop_plan *plan, const void *GY, const v
                                 void *dW, int out_dtype, void *workspace, size_t ws_bytes,
                                 adahop_stream_t stream);
 
+/* Saved context (AdaHOP appendix, IHT and Quantization: the forward pass saves quantised
+ * operands for the backward pass).  The forward pass writes X quantised in the wgrad
+ * orientation (lines = the K columns, blocks along M) and W in the dgrad orientation (lines =
+ * the K columns, blocks along N), each with the zero mask and Hadamard setting that backward
+ * GEMM applies, into a caller-owned device buffer; the backward pass then skips both
+ * quantisations.  Results are bit-identical to adahop_linear_fwd / adahop_linear_bwd.  Where
+ * the forward GEMM quantises the same tensor with the same mask and Hadamard setting, one pass
+ * over it writes both orientations; otherwise the forward call runs the extra pass.  X and W
+ * are still passed to the backward call: outlier extraction reads r of their lines in bf16.
+ *
+ * adahop_saved_size: *bytes receives the buffer size for this plan and shape (0 when both
+ * backward GEMMs use the BF16 strategy).  Layout: X codes (K x M/2), X scales (tensor-core
+ * layout), W codes (K x N/2), W scales, each part 256-byte aligned, present only when that
+ * backward GEMM quantises. */
+adahop_status adahop_saved_size(const adahop_plan *plan, int64_t M, int64_t N, int64_t K,
+                                size_t *bytes);
+
+/* adahop_linear_fwd plus the saved context.  saved: device, 256-byte aligned, >= saved_size
+ * bytes (may be NULL only when that size is 0); ADAHOP_ERR_WORKSPACE if saved_bytes is short.
+ * The buffer must stay untouched until the matching adahop_linear_bwd_saved has run. */
+adahop_status adahop_linear_fwd_save(const adahop_plan *plan, const void *X, const void *W,
+                                     int64_t M, int64_t N, int64_t K, void *Y, int out_dtype,
+                                     void *saved, size_t saved_bytes, void *workspace,
+                                     size_t ws_bytes, adahop_stream_t stream);
+
+/* adahop_linear_bwd reading X / W's backward-orientation operands from the saved context
+ * written by adahop_linear_fwd_save with the same plan, shape, X and W. */
+adahop_status adahop_linear_bwd_saved(const adahop_plan *plan, const void *GY, const void *X,
+                                      const void *W, const void *saved, size_t saved_bytes,
+                                      int64_t M, int64_t N, int64_t K, void *dX, void *dW,
+                                      int out_dtype, void *workspace, size_t ws_bytes,
+                                      adahop_stream_t stream);
+
 /* Waits for the stream, then reads (and clears) the workspace status word.
  * Returns ADAHOP_ERR_TIMEOUT if any kernel that used this workspace gave up a bounded wait. */
 adahop_status adahop_get_device_status(void *workspace, adahop_stream_t stream);

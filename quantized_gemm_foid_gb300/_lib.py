@@ -41,6 +41,14 @@ PROTOTYPES = {
     "adahop_linear_bwd": (c_int, [C.POINTER(AdahopPlan), c_void_p, c_void_p, c_void_p, c_int64,
                                   c_int64, c_int64, c_void_p, c_void_p, c_int, c_void_p, c_size_t,
                                   c_void_p]),
+    "adahop_saved_size": (c_int, [C.POINTER(AdahopPlan), c_int64, c_int64, c_int64,
+                                  C.POINTER(c_size_t)]),
+    "adahop_linear_fwd_save": (c_int, [C.POINTER(AdahopPlan), c_void_p, c_void_p, c_int64, c_int64,
+                                       c_int64, c_void_p, c_int, c_void_p, c_size_t, c_void_p,
+                                       c_size_t, c_void_p]),
+    "adahop_linear_bwd_saved": (c_int, [C.POINTER(AdahopPlan), c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_size_t, c_int64, c_int64, c_int64, c_void_p,
+                                        c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
     "adahop_get_device_status": (c_int, [c_void_p, c_void_p]),
     "adahop_foid": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p,
                             c_void_p, c_size_t, c_void_p]),

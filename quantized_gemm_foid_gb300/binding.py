@@ -111,6 +111,60 @@ def adahop_linear_fwd(plan: AdahopPlan, X, W, Y, workspace, stream=None) -> None
                                  _p(workspace), workspace.numel(), _stream(stream)), "adahop_linear_fwd")
 
 
+def adahop_saved_size(plan: AdahopPlan, M: int, N: int, K: int) -> int:
+    out = C.c_size_t(0)
+    _check(LIB.adahop_saved_size(C.byref(plan), M, N, K, C.byref(out)), "adahop_saved_size")
+    return out.value
+
+
+def new_saved(plan: AdahopPlan, M: int, N: int, K: int, device="cuda") -> torch.Tensor:
+    """A device buffer of adahop_saved_size bytes (uint8) for one layer's saved context."""
+    return torch.empty(max(adahop_saved_size(plan, M, N, K), 256), dtype=torch.uint8, device=device)
+
+
+def adahop_linear_fwd_save(plan: AdahopPlan, X, W, Y, saved, workspace, stream=None) -> None:
+    _cuda(X, "X", torch.bfloat16)
+    _cuda(W, "W", torch.bfloat16)
+    _cuda(Y, "Y")
+    _cuda(saved, "saved", torch.uint8)
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(Y.shape) != (M, N):
+        raise ValueError("shape mismatch: X (M,K), W (N,K), Y (M,N)")
+    _check(LIB.adahop_linear_fwd_save(C.byref(plan), _p(X), _p(W), M, N, K, _p(Y), _out_dtype(Y), _p(saved),
+                                      saved.numel(), _p(workspace), workspace.numel(), _stream(stream)),
+           "adahop_linear_fwd_save")
+
+
+def _bwd_outputs(GY, X, W, dX, dW):
+    _cuda(GY, "GY", torch.bfloat16)
+    _cuda(X, "X", torch.bfloat16)
+    _cuda(W, "W", torch.bfloat16)
+    M, K = X.shape
+    N = W.shape[0]
+    if tuple(GY.shape) != (M, N):
+        raise ValueError("GY must be M x N")
+    outs = [t for t in (dX, dW) if t is not None]
+    if not outs:
+        raise ValueError("at least one of dX, dW")
+    dt = _out_dtype(outs[0])
+    if any(_out_dtype(t) != dt for t in outs):
+        raise TypeError("dX and dW must share a dtype")
+    if dX is not None and tuple(dX.shape) != (M, K):
+        raise ValueError("dX must be M x K")
+    if dW is not None and tuple(dW.shape) != (N, K):
+        raise ValueError("dW must be N x K")
+    return M, N, K, dt
+
+
+def adahop_linear_bwd_saved(plan: AdahopPlan, GY, X, W, saved, dX, dW, workspace, stream=None) -> None:
+    _cuda(saved, "saved", torch.uint8)
+    M, N, K, dt = _bwd_outputs(GY, X, W, dX, dW)
+    _check(LIB.adahop_linear_bwd_saved(C.byref(plan), _p(GY), _p(X), _p(W), _p(saved), saved.numel(), M, N, K,
+                                       _p(dX), _p(dW), dt, _p(workspace), workspace.numel(), _stream(stream)),
+           "adahop_linear_bwd_saved")
+
+
 def adahop_linear_bwd(plan: AdahopPlan, GY, X, W, dX, dW, workspace, stream=None) -> None:
     _cuda(GY, "GY", torch.bfloat16)
     _cuda(X, "X", torch.bfloat16)

@@ -302,9 +302,14 @@ struct PreA {
   uint8_t *codes, *sf;
 };
 
+// pre_a / pre_b: operand already quantised in this GEMM's orientation (codes + tensor-core
+// scales), so its quantisation is skipped.  alt_a / alt_b: the operand is quantised by the
+// dual-orientation pass, which also writes its other orientation (J = the stored rows) there;
+// only valid where the GEMM quantises the stored tensor along its columns (inner axis 1).
 adahop_status run_gemm(const Ctx &cx, int gemm, int strategy, int r, const Tensor t[3],
                        const int pats[3], void *C, int out_dtype, FoidCache *fc,
-                       const PreA *pre_a = nullptr) {
+                       const PreA *pre_a = nullptr, const PreA *pre_b = nullptr,
+                       const PreA *alt_a = nullptr, const PreA *alt_b = nullptr) {
   const GemmShape sh = shape_of(gemm, t[T_X].rows, t[T_W].rows, t[T_X].cols);
   const GemmRoles ro = roles_of(gemm);
   const Tensor &ta = t[ro.a_src];
@@ -332,7 +337,9 @@ adahop_status run_gemm(const Ctx &cx, int gemm, int strategy, int r, const Tenso
   // quantise A (stored tensor ta, orientation a_inner_axis) and B^T (tb, b_inner_axis)
   uint8_t *ac = pre_a ? pre_a->codes : ws + cx.lay.a_codes;
   uint8_t *asf = pre_a ? pre_a->sf : ws + cx.lay.a_sf;
-  uint8_t *bc = ws + cx.lay.b_codes, *bsf = ws + cx.lay.b_sf;
+  uint8_t *bc = pre_b ? pre_b->codes : ws + cx.lay.b_codes;
+  uint8_t *bsf = pre_b ? pre_b->sf : ws + cx.lay.b_sf;
+  if ((alt_a && ro.a_inner_axis != 1) || (alt_b && ro.b_inner_axis != 1)) return ADAHOP_ERR_INVALID_ARG;
   {
     QuantArgs q{};
     q.hadamard = hadamard;
@@ -342,13 +349,21 @@ adahop_status run_gemm(const Ctx &cx, int gemm, int strategy, int r, const Tenso
       q.zero_rows = (oe.tensor == ro.a_src && oe.axis == 0) ? mask : nullptr;
       q.zero_cols = (oe.tensor == ro.a_src && oe.axis == 1) ? mask : nullptr;
       q.codes = ac; q.scales = asf;
-      CUDA_TRY(launch_quant(q, ro.a_inner_axis, cx.num_sms, cx.s), "quantise A");
+      if (alt_a)
+        CUDA_TRY(launch_quant_dual(q, alt_a->codes, alt_a->sf, cx.s), "quantise A (both orientations)");
+      else
+        CUDA_TRY(launch_quant(q, ro.a_inner_axis, cx.num_sms, cx.s), "quantise A");
     }
-    q.T = tb.p; q.rows = tb.rows; q.cols = tb.cols;
-    q.zero_rows = (oe.tensor == ro.b_src && oe.axis == 0) ? mask : nullptr;
-    q.zero_cols = (oe.tensor == ro.b_src && oe.axis == 1) ? mask : nullptr;
-    q.codes = bc; q.scales = bsf;
-    CUDA_TRY(launch_quant(q, ro.b_inner_axis, cx.num_sms, cx.s), "quantise B");
+    if (!pre_b) {
+      q.T = tb.p; q.rows = tb.rows; q.cols = tb.cols;
+      q.zero_rows = (oe.tensor == ro.b_src && oe.axis == 0) ? mask : nullptr;
+      q.zero_cols = (oe.tensor == ro.b_src && oe.axis == 1) ? mask : nullptr;
+      q.codes = bc; q.scales = bsf;
+      if (alt_b)
+        CUDA_TRY(launch_quant_dual(q, alt_b->codes, alt_b->sf, cx.s), "quantise B (both orientations)");
+      else
+        CUDA_TRY(launch_quant(q, ro.b_inner_axis, cx.num_sms, cx.s), "quantise B");
+    }
   }
   if (oe.tensor < 0) return mxf4_gemm(cx, ac, asf, bc, bsf, sh.P, sh.Q, sh.J, nullptr, nullptr, 0, C, out_dtype);
 
@@ -472,6 +487,130 @@ adahop_status linear_common(const adahop_plan *plan, int64_t M, int64_t N, int64
   return ADAHOP_OK;
 }
 
+// Saved context (AdaHOP appendix, IHT and Quantization: the forward pass saves quantised
+// operands for the backward pass).  X quantised in the wgrad orientation (lines = K columns,
+// J = M) and W in the dgrad orientation (lines = K columns, J = N), codes then tensor-core scales,
+// each present only when that backward GEMM quantises (strategy other than BF16).
+struct SavedLayout {
+  bool has_x = false, has_w = false;
+  size_t x_codes = 0, x_sf = 0, w_codes = 0, w_sf = 0, total = 0;
+};
+SavedLayout saved_layout(const adahop_plan *plan, int64_t M, int64_t N, int64_t K) {
+  SavedLayout l;
+  l.has_x = plan->wgrad != ADAHOP_BF16;
+  l.has_w = plan->dgrad != ADAHOP_BF16;
+  size_t off = 0;
+  if (l.has_x) {
+    l.x_codes = off;
+    off += align256(static_cast<size_t>(K * M / 2));
+    l.x_sf = off;
+    off += align256(static_cast<size_t>(K * M / 32));
+  }
+  if (l.has_w) {
+    l.w_codes = off;
+    off += align256(static_cast<size_t>(K * N / 2));
+    l.w_sf = off;
+    off += align256(static_cast<size_t>(K * N / 32));
+  }
+  l.total = off;
+  return l;
+}
+
+// The lines a backward GEMM zeroes in a stored tensor before quantising it: -1 none, else the
+// axis (0 rows, 1 columns) of the tensor whose FOID lines are zeroed.
+int zero_axis(int gemm, int strategy, int r, const int pats[3], int tensor) {
+  if (r <= 0 || (strategy != ADAHOP_OE_LEFT && strategy != ADAHOP_OE_RIGHT)) return -1;
+  const OeChoice c = oe_choice(gemm, strategy, pats);
+  return c.tensor == tensor ? c.axis : -1;
+}
+
+// Quantises one stored tensor into a saved orientation on its own (when the forward pass cannot
+// write it from its own quantisation): FOID on the tensor if the backward GEMM zeroes its lines,
+// then the quantiser along the stored rows (inner axis 0).
+adahop_status quantise_saved(const Ctx &cx, const Tensor &src, int zaxis, int r, int hadamard, uint8_t *codes,
+                             uint8_t *sf) {
+  uint32_t *mask = reinterpret_cast<uint32_t *>(cx.ws + cx.lay.mask);
+  if (zaxis >= 0)
+    CUDA_TRY(launch_foid(src.p, src.rows, src.cols, zaxis, r, reinterpret_cast<int32_t *>(cx.ws + cx.lay.idx), mask,
+                         cx.ws + cx.lay.foid, cx.s),
+             "foid");
+  QuantArgs q{};
+  q.T = src.p; q.rows = src.rows; q.cols = src.cols;
+  q.zero_rows = zaxis == 0 ? mask : nullptr;
+  q.zero_cols = zaxis == 1 ? mask : nullptr;
+  q.codes = codes; q.scales = sf;
+  q.hadamard = hadamard;
+  q.scale_layout = 1;
+  CUDA_TRY(launch_quant(q, 0, cx.num_sms, cx.s), "quantise saved operand");
+  return ADAHOP_OK;
+}
+
+// Backward pass; `saved` (may be null) holds X / W already quantised in the backward orientations.
+adahop_status linear_bwd_impl(const adahop_plan *plan, const void *GY, const void *X, const void *W, int64_t M,
+                              int64_t N, int64_t K, void *dX, void *dW, int out_dtype, void *workspace,
+                              size_t ws_bytes, cudaStream_t s, const uint8_t *saved) {
+  DeviceInfo di;
+  ST_TRY(linear_common(plan, M, N, K, workspace, ws_bytes, &di));
+  const Tensor t[3] = {{static_cast<const uint16_t *>(X), M, K},
+                       {static_cast<const uint16_t *>(W), N, K},
+                       {static_cast<const uint16_t *>(GY), M, N}};
+  const int pats[3] = {plan->x, plan->w, plan->gy};
+  // dgrad and wgrad reuse the workspace in stream order.  Their layouts share the FOID / index /
+  // mask prefix, so when both extract the same lines (e.g. Row-wise G_Y: outer rows for dgrad,
+  // inner rows for wgrad) FOID runs once.
+  const int64_t lines = std::max(std::max(M, N), K);
+  const GemmShape shd = shape_of(1, M, N, K), shw = shape_of(2, M, N, K);
+  const GemmWs ld = gemm_ws(shd.P, shd.Q, shd.J, plan->oe_rank, kSizingSms, lines);
+  const GemmWs lw = gemm_ws(shw.P, shw.Q, shw.J, plan->oe_rank, kSizingSms, lines);
+  FoidCache fc;
+  const bool share = ld.idx == lw.idx && ld.mask == lw.mask;
+  // Prep fusion: when both GEMMs quantise G_Y (dgrad along N, wgrad along M) with the same
+  // Hadamard setting and the same outlier mask, one pass over G_Y writes both orientations.
+  PreA pre_d{}, pre_w{};
+  bool dual = false;
+  if (dX && dW && share) {
+    const int sd = plan->dgrad, sw = plan->wgrad, r = plan->oe_rank;
+    const bool quant_d = sd != ADAHOP_BF16, quant_w = sw != ADAHOP_BF16;
+    const int gmask_d = zero_axis(1, sd, r, pats, T_GY), gmask_w = zero_axis(2, sw, r, pats, T_GY);
+    dual = quant_d && quant_w && ((sd == ADAHOP_MXFP4) == (sw == ADAHOP_MXFP4)) && gmask_d == gmask_w;
+    if (dual) {
+      uint8_t *ws = static_cast<uint8_t *>(workspace);
+      uint32_t *mask = reinterpret_cast<uint32_t *>(ws + ld.mask);
+      if (gmask_d >= 0) {
+        CUDA_TRY(launch_foid(t[T_GY].p, M, N, gmask_d, r, reinterpret_cast<int32_t *>(ws + ld.idx), mask,
+                             ws + ld.foid, s),
+                 "foid");
+        fc = FoidCache{T_GY, gmask_d, r};
+      }
+      const size_t alt = bwd_alt_offset(M, N, K, r);
+      pre_d = PreA{ws + ld.a_codes, ws + ld.a_sf};
+      pre_w = PreA{ws + alt, ws + alt + align256(static_cast<size_t>(M * N / 2))};
+      QuantArgs q{};
+      q.T = t[T_GY].p; q.rows = M; q.cols = N;
+      q.zero_rows = gmask_d == 0 ? mask : nullptr;
+      q.zero_cols = gmask_d == 1 ? mask : nullptr;
+      q.codes = pre_d.codes; q.scales = pre_d.sf;
+      q.hadamard = sd != ADAHOP_MXFP4;
+      q.scale_layout = 1;
+      CUDA_TRY(launch_quant_dual(q, pre_w.codes, pre_w.sf, s), "quantise G_Y (both orientations)");
+    }
+  }
+  const SavedLayout sl = saved ? saved_layout(plan, M, N, K) : SavedLayout{};
+  uint8_t *sv = const_cast<uint8_t *>(saved);
+  const PreA saved_w{sv + sl.w_codes, sv + sl.w_sf}, saved_x{sv + sl.x_codes, sv + sl.x_sf};
+  if (dX) {
+    Ctx cx{s, static_cast<uint8_t *>(workspace), ld, di.num_sms};
+    ST_TRY(run_gemm(cx, 1, plan->dgrad, plan->oe_rank, t, pats, dX, out_dtype, share ? &fc : nullptr,
+                    dual ? &pre_d : nullptr, sl.has_w ? &saved_w : nullptr));
+  }
+  if (dW) {
+    Ctx cx{s, static_cast<uint8_t *>(workspace), lw, di.num_sms};
+    ST_TRY(run_gemm(cx, 2, plan->wgrad, plan->oe_rank, t, pats, dW, out_dtype, share ? &fc : nullptr,
+                    dual ? &pre_w : nullptr, sl.has_x ? &saved_x : nullptr));
+  }
+  return ADAHOP_OK;
+}
+
 }  // namespace
 
 // =====================================================================================
@@ -563,66 +702,74 @@ adahop_status adahop_linear_bwd(const adahop_plan *plan, const void *GY, const v
   if (out_dtype != ADAHOP_OUT_BF16 && out_dtype != ADAHOP_OUT_FP32) return ADAHOP_ERR_INVALID_ARG;
   if (!aligned(GY, 16) || !aligned(X, 16) || !aligned(W, 16) || (dX && !aligned(dX, 16)) || (dW && !aligned(dW, 16)))
     return ADAHOP_ERR_ALIGN;
+  return linear_bwd_impl(plan, GY, X, W, M, N, K, dX, dW, out_dtype, workspace, ws_bytes,
+                         reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+adahop_status adahop_saved_size(const adahop_plan *plan, int64_t M, int64_t N, int64_t K, size_t *bytes) {
+  if (!bytes) return ADAHOP_ERR_INVALID_ARG;
+  ST_TRY(check_plan(plan));
+  ST_TRY(check_shapes(M, N, K));
+  *bytes = saved_layout(plan, M, N, K).total;
+  return ADAHOP_OK;
+}
+
+adahop_status adahop_linear_fwd_save(const adahop_plan *plan, const void *X, const void *W, int64_t M, int64_t N,
+                                     int64_t K, void *Y, int out_dtype, void *saved, size_t saved_bytes,
+                                     void *workspace, size_t ws_bytes, adahop_stream_t stream) {
+  if (!X || !W || !Y) return ADAHOP_ERR_INVALID_ARG;
+  if (out_dtype != ADAHOP_OUT_BF16 && out_dtype != ADAHOP_OUT_FP32) return ADAHOP_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(Y, 16)) return ADAHOP_ERR_ALIGN;
   DeviceInfo di;
   ST_TRY(linear_common(plan, M, N, K, workspace, ws_bytes, &di));
-  const Tensor t[3] = {{static_cast<const uint16_t *>(X), M, K},
-                       {static_cast<const uint16_t *>(W), N, K},
-                       {static_cast<const uint16_t *>(GY), M, N}};
+  const SavedLayout sl = saved_layout(plan, M, N, K);
+  if (sl.total > 0 && !saved) return ADAHOP_ERR_INVALID_ARG;
+  if (saved && !aligned(saved, 256)) return ADAHOP_ERR_ALIGN;
+  if (saved_bytes < sl.total) return ADAHOP_ERR_WORKSPACE;
+  const GemmShape sh = shape_of(0, M, N, K);
+  Ctx cx{reinterpret_cast<cudaStream_t>(stream), static_cast<uint8_t *>(workspace),
+         gemm_ws(sh.P, sh.Q, sh.J, plan->oe_rank, kSizingSms, std::max(std::max(M, N), K)), di.num_sms};
+  const Tensor t[3] = {{static_cast<const uint16_t *>(X), M, K}, {static_cast<const uint16_t *>(W), N, K}, {nullptr, M, N}};
   const int pats[3] = {plan->x, plan->w, plan->gy};
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // dgrad and wgrad reuse the workspace in stream order.  Their layouts share the FOID / index /
-  // mask prefix, so when both extract the same lines (e.g. Row-wise G_Y: outer rows for dgrad,
-  // inner rows for wgrad) FOID runs once.
-  const int64_t lines = std::max(std::max(M, N), K);
-  const GemmShape shd = shape_of(1, M, N, K), shw = shape_of(2, M, N, K);
-  const GemmWs ld = gemm_ws(shd.P, shd.Q, shd.J, plan->oe_rank, kSizingSms, lines);
-  const GemmWs lw = gemm_ws(shw.P, shw.Q, shw.J, plan->oe_rank, kSizingSms, lines);
-  FoidCache fc;
-  const bool share = ld.idx == lw.idx && ld.mask == lw.mask;
-  // Prep fusion: when both GEMMs quantise G_Y (dgrad along N, wgrad along M) with the same
-  // Hadamard setting and the same outlier mask, one pass over G_Y writes both orientations.
-  PreA pre_d{}, pre_w{};
-  bool dual = false;
-  if (dX && dW && share) {
-    const int sd = plan->dgrad, sw = plan->wgrad, r = plan->oe_rank;
-    const bool quant_d = sd != ADAHOP_BF16, quant_w = sw != ADAHOP_BF16;
-    const OeChoice od = (r > 0 && (sd == ADAHOP_OE_LEFT || sd == ADAHOP_OE_RIGHT)) ? oe_choice(1, sd, pats) : OeChoice{};
-    const OeChoice ow = (r > 0 && (sw == ADAHOP_OE_LEFT || sw == ADAHOP_OE_RIGHT)) ? oe_choice(2, sw, pats) : OeChoice{};
-    const int gmask_d = od.tensor == T_GY ? od.axis : -1, gmask_w = ow.tensor == T_GY ? ow.axis : -1;
-    dual = quant_d && quant_w && ((sd == ADAHOP_MXFP4) == (sw == ADAHOP_MXFP4)) && gmask_d == gmask_w;
-    if (dual) {
-      uint8_t *ws = static_cast<uint8_t *>(workspace);
-      uint32_t *mask = reinterpret_cast<uint32_t *>(ws + ld.mask);
-      if (gmask_d >= 0) {
-        CUDA_TRY(launch_foid(t[T_GY].p, M, N, gmask_d, r, reinterpret_cast<int32_t *>(ws + ld.idx), mask,
-                             ws + ld.foid, s),
-                 "foid");
-        fc = FoidCache{T_GY, gmask_d, r};
-      }
-      const size_t alt = bwd_alt_offset(M, N, K, r);
-      pre_d = PreA{ws + ld.a_codes, ws + ld.a_sf};
-      pre_w = PreA{ws + alt, ws + alt + align256(static_cast<size_t>(M * N / 2))};
-      QuantArgs q{};
-      q.T = t[T_GY].p; q.rows = M; q.cols = N;
-      q.zero_rows = gmask_d == 0 ? mask : nullptr;
-      q.zero_cols = gmask_d == 1 ? mask : nullptr;
-      q.codes = pre_d.codes; q.scales = pre_d.sf;
-      q.hadamard = sd != ADAHOP_MXFP4;
-      q.scale_layout = 1;
-      CUDA_TRY(launch_quant_dual(q, pre_w.codes, pre_w.sf, s), "quantise G_Y (both orientations)");
-    }
-  }
-  if (dX) {
-    Ctx cx{s, static_cast<uint8_t *>(workspace), ld, di.num_sms};
-    ST_TRY(run_gemm(cx, 1, plan->dgrad, plan->oe_rank, t, pats, dX, out_dtype, share ? &fc : nullptr,
-                    dual ? &pre_d : nullptr));
-  }
-  if (dW) {
-    Ctx cx{s, static_cast<uint8_t *>(workspace), lw, di.num_sms};
-    ST_TRY(run_gemm(cx, 2, plan->wgrad, plan->oe_rank, t, pats, dW, out_dtype, share ? &fc : nullptr,
-                    dual ? &pre_w : nullptr));
-  }
+  const int r = plan->oe_rank;
+  uint8_t *sv = static_cast<uint8_t *>(saved);
+  const PreA save_x{sv + sl.x_codes, sv + sl.x_sf}, save_w{sv + sl.w_codes, sv + sl.w_sf};
+  // X (wgrad's B) and W (dgrad's B) need, in the backward orientation, the zero mask and Hadamard
+  // setting of that backward GEMM.  Where those equal the forward GEMM's, the forward
+  // quantisation writes both orientations in one pass.
+  const int zx_f = zero_axis(0, plan->fwd, r, pats, T_X), zw_f = zero_axis(0, plan->fwd, r, pats, T_W);
+  const int zx_b = zero_axis(2, plan->wgrad, r, pats, T_X), zw_b = zero_axis(1, plan->dgrad, r, pats, T_W);
+  const bool fwd_quant = plan->fwd != ADAHOP_BF16;
+  const bool had_f = plan->fwd != ADAHOP_MXFP4;
+  const bool dual_x = sl.has_x && fwd_quant && zx_f == zx_b && had_f == (plan->wgrad != ADAHOP_MXFP4);
+  const bool dual_w = sl.has_w && fwd_quant && zw_f == zw_b && had_f == (plan->dgrad != ADAHOP_MXFP4);
+  ST_TRY(run_gemm(cx, 0, plan->fwd, r, t, pats, Y, out_dtype, nullptr, nullptr, nullptr, dual_x ? &save_x : nullptr,
+                  dual_w ? &save_w : nullptr));
+  if (sl.has_x && !dual_x)
+    ST_TRY(quantise_saved(cx, t[T_X], zx_b, r, plan->wgrad != ADAHOP_MXFP4, save_x.codes, save_x.sf));
+  if (sl.has_w && !dual_w)
+    ST_TRY(quantise_saved(cx, t[T_W], zw_b, r, plan->dgrad != ADAHOP_MXFP4, save_w.codes, save_w.sf));
   return ADAHOP_OK;
+}
+
+adahop_status adahop_linear_bwd_saved(const adahop_plan *plan, const void *GY, const void *X, const void *W,
+                                      const void *saved, size_t saved_bytes, int64_t M, int64_t N, int64_t K,
+                                      void *dX, void *dW, int out_dtype, void *workspace, size_t ws_bytes,
+                                      adahop_stream_t stream) {
+  if (!GY || !X || !W || (!dX && !dW)) return ADAHOP_ERR_INVALID_ARG;
+  if (out_dtype != ADAHOP_OUT_BF16 && out_dtype != ADAHOP_OUT_FP32) return ADAHOP_ERR_INVALID_ARG;
+  if (!aligned(GY, 16) || !aligned(X, 16) || !aligned(W, 16) || (dX && !aligned(dX, 16)) || (dW && !aligned(dW, 16)))
+    return ADAHOP_ERR_ALIGN;
+  ST_TRY(check_plan(plan));
+  ST_TRY(check_shapes(M, N, K));
+  const SavedLayout sl = saved_layout(plan, M, N, K);
+  if (sl.total > 0 && !saved) return ADAHOP_ERR_INVALID_ARG;
+  if (saved && !aligned(saved, 256)) return ADAHOP_ERR_ALIGN;
+  if (saved_bytes < sl.total) return ADAHOP_ERR_WORKSPACE;
+  static const uint8_t kNone = 0;
+  return linear_bwd_impl(plan, GY, X, W, M, N, K, dX, dW, out_dtype, workspace, ws_bytes,
+                         reinterpret_cast<cudaStream_t>(stream),
+                         saved ? static_cast<const uint8_t *>(saved) : &kNone);
 }
 
 adahop_status adahop_get_device_status(void *workspace, adahop_stream_t stream) {

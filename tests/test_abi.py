@@ -89,3 +89,17 @@ def test_python_binding_names_match_c(lib):
         if name in ("adahop_status_string", "adahop_last_cuda_error"):
             continue
         assert callable(getattr(b, name)), name
+
+
+def test_saved_size_layout(lib):
+    q = lib
+    IHT, BF16 = 0, 3
+    M, N, K = 512, 256, 384
+    a = lambda v: (v + 255) // 256 * 256
+    full = a(K * M // 2) + a(K * M // 32) + a(K * N // 2) + a(K * N // 32)
+    assert q.adahop_saved_size(q.make_plan(fwd=IHT, dgrad=IHT, wgrad=IHT), M, N, K) == full
+    assert q.adahop_saved_size(q.make_plan(dgrad=BF16, wgrad=IHT), M, N, K) == a(K * M // 2) + a(K * M // 32)
+    assert q.adahop_saved_size(q.make_plan(dgrad=BF16, wgrad=BF16), M, N, K) == 0
+    # compression of the saved activation against its bf16 copy: 2 / (1/2 + 1/32) bytes per element
+    x_part = a(K * M // 2) + a(K * M // 32)
+    assert 2 * M * K / x_part == pytest.approx(2 / (0.5 + 1 / 32), rel=1e-3)
