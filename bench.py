@@ -574,6 +574,18 @@ def profile(q, device, args):
         print(f"profiled one step: {b.launches_per_step()} launches")
         return
     from synthetic import normal_bf16
+    if args.profile == "quant":
+        M, N = 32768, 14336                             # G_Y of the gate projection
+        G = normal_bf16(M, N, 1e-3, 3, device=device)
+        cr = torch.empty(M * N // 2, dtype=torch.uint8, device=device)
+        sr = torch.empty(M * N // 32, dtype=torch.uint8, device=device)
+        cc = torch.empty(M * N // 2, dtype=torch.uint8, device=device)
+        sc = torch.empty(M * N // 32, dtype=torch.uint8, device=device)
+        for _ in range(3):
+            q.adahop_quantize_mxfp4_dual(G, 1, None, None, cr, sr, cc, sc, 1)
+        torch.cuda.synchronize()
+        print("profiled 3 dual-orientation quantiser launches")
+        return
     P, Q, J = 32768, 4096, 14336
     A = normal_bf16(P, J, 1e-3, 1, device=device)
     B = normal_bf16(J, Q, 0.02, 2, device=device)      # W (N x K), quantised along N
@@ -603,10 +615,11 @@ def main():
     ap.add_argument("--sweep-m", default=None, help="comma-separated M values for --sweep")
     ap.add_argument("--quality", action="store_true",
                     help="relative MSE of the Table 3 plans on the 8B gate projection; prints one JSON object")
-    ap.add_argument("--profile", choices=["step", "gemm"], default=None,
+    ap.add_argument("--profile", choices=["step", "gemm", "quant"], default=None,
                     help="for ncu only (prints no bench line): 'step' = warm-up steps then one step "
                          "of the workload; 'gemm' = three launches of the fused MXFP4 GEMM on the "
-                         "dgrad shape P=32768, Q=4096, J=14336")
+                         "dgrad shape P=32768, Q=4096, J=14336; 'quant' = three launches of the "
+                         "dual-orientation quantiser on the 32768 x 14336 G_Y")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

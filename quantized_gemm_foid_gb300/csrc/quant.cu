@@ -16,7 +16,10 @@
 //     negative values that round to zero give 0x8) -- exactly what cvt.rn.satfinite.e2m1x2.f32
 //     computes, two elements per instruction;
 //   * an all-zero block stores byte 0 and codes 0.
-// Work distribution (HBM-bound: 2 B read + 0.53 B written per element):
+// The transform and scaling run on packed float32 pairs (add/sub/mul.rn.f32x2, each lane rounded
+// as the scalar instruction), which halves the float32 instruction count of the butterflies; at
+// HBM rate the two-orientation pass is otherwise bound by float32 issue, not by memory.
+// Work distribution (2 B read + 0.53 B written per element and orientation):
 //   rows kernel: J = columns.  One thread per 32-block: four 16-byte loads, all five butterfly
 //                stages in registers, one 16-byte code store (a warp stores 512 contiguous bytes).
 //   cols kernel: J = rows (the transposed orientation).  A 128 x 128 tile is staged in shared
@@ -68,43 +71,100 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
   return out;
 }
 
-__device__ __forceinline__ void butterfly(float &a, float &b) {
-  const float s = __fadd_rn(a, b);
-  const float d = __fsub_rn(a, b);
-  a = s;
-  b = d;
+// Two float32 lanes in one 64-bit register: the packed add / sub / mul instructions round each
+// lane exactly like the scalar float32 instruction (round to nearest even, no flush to zero).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
-// The orthonormal block-32 Sylvester Hadamard in place (stride 1, 2, 4, 8, 16, then scale).
-__device__ __forceinline__ void fwht32(float (&x)[32]) {
+// Quantises one 32-block held in registers (x[i] = element i, zeroed lines already +0):
+// optional orthonormal block-32 Sylvester Hadamard (butterflies with stride 1, 2, 4, 8, 16, each
+// (a, b) -> (a + b, a - b) rounded to float32, then * c), E8M0 scale from the block amax, E2M1
+// codes.  Returns the scale byte and writes 16 code bytes (element i in nibble i).
+//
+// The block lives in 16 packed registers p[k] = (x_k, x_{k+16}): the stride 1..8 butterflies
+// pair p[k] with p[k + h] and run two at a time; stride 16 pairs the two lanes of p[k].  Every
+// lane sees the same operands in the same order as the scalar definition, so the results are
+// identical.  Scaling: with y the transformed block, the definition computes
+// v = RN(RN(y c) s), s = 2^(127 - byte), and amax = max |RN(y c)| = RN(max |y| c) (rounding is
+// monotonic and odd).  Where 2^-100 <= amax <= 2^100, c s is an exact normal float32 and
+// RN(y (c s)) equals RN(RN(y c) s) for every y with |y c| >= 2^-126 (power-of-two scaling of
+// normal floats is exact and commutes with rounding); smaller |y c| give |v| <= 2^-24 either way,
+// i.e. a signed zero code.  So one multiply replaces two there; elsewhere both are done.
+__device__ __forceinline__ uint32_t quantize32(const float (&x)[32], int hadamard, uint4 &codes) {
+  uint64_t p[16];
 #pragma unroll
-  for (int h = 1; h < 32; h <<= 1) {
+  for (int k = 0; k < 16; ++k) p[k] = pack2(x[k], x[k + 16]);
+  if (hadamard) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if ((i & h) == 0) butterfly(x[i], x[i + h]);
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if ((k & h) == 0) {
+          const uint64_t a = p[k], b = p[k + h];
+          p[k] = add2(a, b);
+          p[k + h] = sub2(a, b);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      float lo, hi;
+      unpack2(p[k], lo, hi);
+      p[k] = pack2(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
+    }
   }
-  const float c = inv_sqrt32();
-#pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], c);
-}
-
-// Quantises one 32-block in registers: returns the scale byte and writes 16 code bytes.
-__device__ __forceinline__ uint32_t quantize_block(float (&x)[32], uint4 &codes) {
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const uint32_t byte = mx_scale_byte(amax);
-  if (amax > 0.0f) {
-    const float s = mx_inv_scale(byte);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], s);
-    codes.x = e2m1x8(x[0], x[1], x[2], x[3], x[4], x[5], x[6], x[7]);
-    codes.y = e2m1x8(x[8], x[9], x[10], x[11], x[12], x[13], x[14], x[15]);
-    codes.z = e2m1x8(x[16], x[17], x[18], x[19], x[20], x[21], x[22], x[23]);
-    codes.w = e2m1x8(x[24], x[25], x[26], x[27], x[28], x[29], x[30], x[31]);
-  } else {
-    codes = make_uint4(0u, 0u, 0u, 0u);
+  for (int k = 0; k < 16; ++k) {
+    float lo, hi;
+    unpack2(p[k], lo, hi);
+    amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
   }
+  const float c = inv_sqrt32();
+  if (hadamard) amax = __fmul_rn(amax, c);
+  const uint32_t byte = mx_scale_byte(amax);
+  if (!(amax > 0.0f)) {
+    codes = make_uint4(0u, 0u, 0u, 0u);
+    return byte;
+  }
+  const float s = mx_inv_scale(byte);
+  if (hadamard && !(amax >= 0x1p-100f && amax <= 0x1p100f)) {
+    const uint64_t cc = pack2(c, c);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) p[k] = mul2(p[k], cc);
+  }
+  const float m = (hadamard && amax >= 0x1p-100f && amax <= 0x1p100f) ? __fmul_rn(c, s) : s;
+  const uint64_t mm = pack2(m, m);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) p[k] = mul2(p[k], mm);
+  float v[32];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) unpack2(p[k], v[k], v[k + 16]);
+  codes.x = e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+  codes.y = e2m1x8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
+  codes.z = e2m1x8(v[16], v[17], v[18], v[19], v[20], v[21], v[22], v[23]);
+  codes.w = e2m1x8(v[24], v[25], v[26], v[27], v[28], v[29], v[30], v[31]);
   return byte;
 }
 
@@ -138,14 +198,13 @@ __device__ __forceinline__ void quant_rows_block(const QuantArgs &a, int64_t blk
     for (int i = 0; i < 32; ++i)
       if ((zmask >> i) & 1u) x[i] = 0.0f;
   }
-  if (a.hadamard) fwht32(x);
   uint4 codes;
-  const uint32_t byte = quantize_block(x, codes);
+  const uint32_t byte = quantize32(x, a.hadamard, codes);
   *reinterpret_cast<uint4 *>(a.codes + row * (J >> 1) + (blk << 4)) = codes;
   a.scales[scale_offset(a.scale_layout, row, blk, J)] = static_cast<uint8_t>(byte);
 }
 
-__global__ void __launch_bounds__(256) quant_rows_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(256, 3) quant_rows_kernel(QuantArgs a) {
   const int64_t total = a.rows * (a.cols >> 5);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -169,20 +228,23 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantArgs a) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// cols kernel: lines = columns of T, J = rows.  Tile 128 rows x 128 cols, 256 threads; thread t
-// takes the column pair (2 (t % 64), 2 (t % 64) + 1) and the 32-row block t / 64.
+// cols kernel: lines = columns of T, J = rows.  Tile 64 rows x 128 cols, 128 threads; thread t
+// takes the column pair (2 (t % 64), 2 (t % 64) + 1) and the 32-row block t / 64.  Small tiles
+// let six CTAs share an SM, so that some load while others compute.
 // ---------------------------------------------------------------------------------------------
-constexpr int kColTile = 128;
+constexpr int kColTile = 128;                     // columns per tile
+constexpr int kTileRows = 64;                     // rows per tile (two 32-row blocks)
+constexpr int kTileThreads = 128;
 
-__global__ void __launch_bounds__(256, 3) quant_cols_kernel(QuantArgs a) {
-  __shared__ __align__(16) uint32_t tile[kColTile][kColTile / 2];   // bf16 pairs
+__global__ void __launch_bounds__(kTileThreads, 6) quant_cols_kernel(QuantArgs a) {
+  __shared__ __align__(16) uint32_t tile[kTileRows][kColTile / 2];   // bf16 pairs
   const int64_t R = a.rows, C = a.cols;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColTile;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTileRows;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kColTile;
   const int tid = threadIdx.x;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {                   // 2048 chunks of 16 B, 16 per tile row
-    const int chunk = tid + 256 * k;
+  for (int k = 0; k < 8; ++k) {                   // 1024 chunks of 16 B, 16 per tile row
+    const int chunk = tid + kTileThreads * k;
     const int row = chunk >> 4, cc = (chunk & 15) << 2;   // cc in 32-bit words
     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * C + c0) + (chunk & 15));
     *reinterpret_cast<uint4 *>(&tile[row][cc]) = v;
@@ -209,31 +271,31 @@ __global__ void __launch_bounds__(256, 3) quant_cols_kernel(QuantArgs a) {
       for (int i = 0; i < 32; ++i)
         if ((zmask >> i) & 1u) x[i] = 0.0f;
     }
-    if (a.hadamard) fwht32(x);
     uint4 codes;
-    const uint32_t byte = quantize_block(x, codes);
+    const uint32_t byte = quantize32(x, a.hadamard, codes);
     *reinterpret_cast<uint4 *>(a.codes + line * (R >> 1) + (blk << 4)) = codes;
     a.scales[scale_offset(a.scale_layout, line, blk, R)] = static_cast<uint8_t>(byte);
   }
 }
 
 // ---------------------------------------------------------------------------------------------
-// dual kernel: both orientations of one tensor from a single read (prep fusion).  Tile 128 x 128
-// staged in shared memory with 4-word row padding (conflict-free row reads and column-pair
-// reads); each thread quantises two 32-blocks along the tile's rows (J = cols) and one 32-row
-// block of each column of a column pair (J = rows).  Same arithmetic as the two kernels above.
+// dual kernel: both orientations of one tensor from a single read (prep fusion).  Tile 64 rows x
+// 128 cols staged in shared memory with 4-word row padding (conflict-free row reads and
+// column-pair reads), 128 threads, six CTAs per SM; each thread quantises two 32-blocks along the
+// tile's rows (J = cols) and one 32-row block of each column of a column pair (J = rows).  Same
+// arithmetic as the two kernels above.
 // ---------------------------------------------------------------------------------------------
 constexpr int kDualPitch = kColTile / 2 + 4;     // 32-bit words per staged row
 
-__global__ void __launch_bounds__(256, 3) quant_dual_kernel(QuantArgs a, uint8_t *codes_c, uint8_t *scales_c) {
-  __shared__ __align__(16) uint32_t tile[kColTile][kDualPitch];
+__global__ void __launch_bounds__(kTileThreads, 6) quant_dual_kernel(QuantArgs a, uint8_t *codes_c, uint8_t *scales_c) {
+  __shared__ __align__(16) uint32_t tile[kTileRows][kDualPitch];
   const int64_t R = a.rows, C = a.cols;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColTile;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTileRows;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kColTile;
   const int tid = threadIdx.x;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const int chunk = tid + 256 * k;
+    const int chunk = tid + kTileThreads * k;
     const int row = chunk >> 4, cc = (chunk & 15) << 2;
     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * C + c0) + (chunk & 15));
     *reinterpret_cast<uint4 *>(&tile[row][cc]) = v;
@@ -266,9 +328,8 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(QuantArgs a, uint8_t
         for (int i = 0; i < 32; ++i)
           if ((zmask >> i) & 1u) x[i] = 0.0f;
       }
-      if (a.hadamard) fwht32(x);
       uint4 codes;
-      const uint32_t byte = quantize_block(x, codes);
+      const uint32_t byte = quantize32(x, a.hadamard, codes);
       *reinterpret_cast<uint4 *>(a.codes + row * (C >> 1) + (blk << 4)) = codes;
       a.scales[scale_offset(a.scale_layout, row, blk, C)] = static_cast<uint8_t>(byte);
     }
@@ -296,9 +357,8 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(QuantArgs a, uint8_t
         for (int i = 0; i < 32; ++i)
           if ((zmask >> i) & 1u) x[i] = 0.0f;
       }
-      if (a.hadamard) fwht32(x);
       uint4 codes;
-      const uint32_t byte = quantize_block(x, codes);
+      const uint32_t byte = quantize32(x, a.hadamard, codes);
       *reinterpret_cast<uint4 *>(codes_c + line * (R >> 1) + (blk << 4)) = codes;
       scales_c[scale_offset(a.scale_layout, line, blk, R)] = static_cast<uint8_t>(byte);
     }
@@ -308,8 +368,8 @@ __global__ void __launch_bounds__(256, 3) quant_dual_kernel(QuantArgs a, uint8_t
 }  // namespace
 
 cudaError_t launch_quant_dual(const QuantArgs &a, uint8_t *codes_cols, uint8_t *scales_cols, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(a.cols / kColTile), static_cast<unsigned>(a.rows / kColTile));
-  quant_dual_kernel<<<grid, 256, 0, s>>>(a, codes_cols, scales_cols);
+  dim3 grid(static_cast<unsigned>(a.cols / kColTile), static_cast<unsigned>(a.rows / kTileRows));
+  quant_dual_kernel<<<grid, kTileThreads, 0, s>>>(a, codes_cols, scales_cols);
   return cudaGetLastError();
 }
 
@@ -321,8 +381,8 @@ cudaError_t launch_quant(const QuantArgs &a, int inner_axis, int num_sms, cudaSt
     if (blocks > cap) blocks = cap;
     quant_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
   } else {
-    dim3 grid(static_cast<unsigned>(a.cols / kColTile), static_cast<unsigned>(a.rows / kColTile));
-    quant_cols_kernel<<<grid, 256, 0, s>>>(a);
+    dim3 grid(static_cast<unsigned>(a.cols / kColTile), static_cast<unsigned>(a.rows / kTileRows));
+    quant_cols_kernel<<<grid, kTileThreads, 0, s>>>(a);
   }
   return cudaGetLastError();
 }
