@@ -97,6 +97,95 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   return r;
 }
 
+// Quantises two 32-blocks side by side: p[i] holds element i of block A in its low lane and
+// element i of block B in its high lane (zeroed lines already +0).  Per block: optional
+// orthonormal block-32 Sylvester Hadamard (butterflies with stride 1, 2, 4, 8, 16, each
+// (a, b) -> (a + b, a - b) rounded to float32, then * c), E8M0 scale from the block amax, E2M1
+// codes; byte_a / byte_b receive the scale bytes, codes_a / codes_b 16 code bytes (element i in
+// nibble i).  An all-zero block gives byte 0 and codes 0.
+//
+// Every lane sees the same operands in the same order as the scalar definition, so the results
+// are identical to it.  Scaling: with y the transformed block, the definition computes
+// v = RN(RN(y c) s), s = 2^(127 - byte), and amax = max |RN(y c)| = RN(max |y| c) (rounding is
+// monotonic and odd).  Where 2^-100 <= amax <= 2^100, c s is an exact normal float32 and
+// RN(y (c s)) equals RN(RN(y c) s) for every y with |y c| >= 2^-126 (power-of-two scaling of
+// normal floats is exact and commutes with rounding); smaller |y c| give |v| <= 2^-24 either way,
+// i.e. a signed zero code.  So one multiply replaces two there; elsewhere both are done (the
+// other lane is multiplied by 1, which is exact).
+__device__ __forceinline__ void quantize32x2(uint64_t (&p)[32], int hadamard, uint4 &codes_a, uint4 &codes_b,
+                                             uint32_t &byte_a, uint32_t &byte_b) {
+  if (hadamard) {
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if ((i & h) == 0) {
+          const uint64_t u = p[i], w = p[i + h];
+          p[i] = add2(u, w);
+          p[i + h] = sub2(u, w);
+        }
+      }
+    }
+  }
+  float amax_a = 0.0f, amax_b = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float lo, hi;
+    unpack2(p[i], lo, hi);
+    amax_a = fmaxf(amax_a, fabsf(lo));
+    amax_b = fmaxf(amax_b, fabsf(hi));
+  }
+  const float c = inv_sqrt32();
+  if (hadamard) {
+    amax_a = __fmul_rn(amax_a, c);
+    amax_b = __fmul_rn(amax_b, c);
+  }
+  byte_a = mx_scale_byte(amax_a);
+  byte_b = mx_scale_byte(amax_b);
+  const float s_a = mx_inv_scale(byte_a), s_b = mx_inv_scale(byte_b);
+  const bool fast_a = amax_a >= 0x1p-100f && amax_a <= 0x1p100f;
+  const bool fast_b = amax_b >= 0x1p-100f && amax_b <= 0x1p100f;
+  float m_a = s_a, m_b = s_b;
+  if (hadamard) {
+    if (!fast_a || !fast_b) {
+      const uint64_t pre = pack2(fast_a ? 1.0f : c, fast_b ? 1.0f : c);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) p[i] = mul2(p[i], pre);
+    }
+    if (fast_a) m_a = __fmul_rn(c, s_a);
+    if (fast_b) m_b = __fmul_rn(c, s_b);
+  }
+  const uint64_t mm = pack2(m_a, m_b);
+  float va[32], vb[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) unpack2(mul2(p[i], mm), va[i], vb[i]);
+  if (amax_a > 0.0f) {
+    codes_a.x = e2m1x8(va[0], va[1], va[2], va[3], va[4], va[5], va[6], va[7]);
+    codes_a.y = e2m1x8(va[8], va[9], va[10], va[11], va[12], va[13], va[14], va[15]);
+    codes_a.z = e2m1x8(va[16], va[17], va[18], va[19], va[20], va[21], va[22], va[23]);
+    codes_a.w = e2m1x8(va[24], va[25], va[26], va[27], va[28], va[29], va[30], va[31]);
+  } else {
+    codes_a = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (amax_b > 0.0f) {
+    codes_b.x = e2m1x8(vb[0], vb[1], vb[2], vb[3], vb[4], vb[5], vb[6], vb[7]);
+    codes_b.y = e2m1x8(vb[8], vb[9], vb[10], vb[11], vb[12], vb[13], vb[14], vb[15]);
+    codes_b.z = e2m1x8(vb[16], vb[17], vb[18], vb[19], vb[20], vb[21], vb[22], vb[23]);
+    codes_b.w = e2m1x8(vb[24], vb[25], vb[26], vb[27], vb[28], vb[29], vb[30], vb[31]);
+  } else {
+    codes_b = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Zeroes the elements of a block whose bit is set in zmask (element i <-> bit i).
+__device__ __forceinline__ void apply_zero_mask(float (&x)[32], uint32_t zmask) {
+  if (zmask) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((zmask >> i) & 1u) x[i] = 0.0f;
+  }
+}
+
 // Quantises one 32-block held in registers (x[i] = element i, zeroed lines already +0):
 // optional orthonormal block-32 Sylvester Hadamard (butterflies with stride 1, 2, 4, 8, 16, each
 // (a, b) -> (a + b, a - b) rounded to float32, then * c), E8M0 scale from the block amax, E2M1
@@ -173,14 +262,13 @@ __device__ __forceinline__ int64_t scale_offset(int layout, int64_t line, int64_
 }
 
 // ---------------------------------------------------------------------------------------------
-// rows kernel: lines = rows of T, J = cols; one thread per 32-block.
+// rows kernel: lines = rows of T, J = cols; each thread transforms two 32-blocks (b and
+// b + stride of the grid-stride loop) side by side.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void quant_rows_block(const QuantArgs &a, int64_t blkid, const uint4 (&raw)[4]) {
-  const int64_t J = a.cols;
-  const int64_t bpr = J >> 5;                  // 32-blocks per row
+__device__ __forceinline__ void load_row_block(const QuantArgs &a, int64_t blkid, const uint4 (&raw)[4], float (&x)[32]) {
+  const int64_t bpr = a.cols >> 5;             // 32-blocks per row
   const int64_t row = blkid / bpr;
   const int64_t blk = blkid - row * bpr;
-  float x[32];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
@@ -193,18 +281,37 @@ __device__ __forceinline__ void quant_rows_block(const QuantArgs &a, int64_t blk
   uint32_t zmask = 0;
   if (a.zero_rows && ((a.zero_rows[row >> 5] >> (row & 31)) & 1u)) zmask = 0xFFFFFFFFu;
   if (a.zero_cols) zmask |= a.zero_cols[blk];          // bits of columns 32*blk .. 32*blk+31
-  if (zmask) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if ((zmask >> i) & 1u) x[i] = 0.0f;
-  }
-  uint4 codes;
-  const uint32_t byte = quantize32(x, a.hadamard, codes);
+  apply_zero_mask(x, zmask);
+}
+
+__device__ __forceinline__ void store_row_block(const QuantArgs &a, int64_t blkid, const uint4 &codes, uint32_t byte) {
+  const int64_t J = a.cols;
+  const int64_t bpr = J >> 5;
+  const int64_t row = blkid / bpr;
+  const int64_t blk = blkid - row * bpr;
   *reinterpret_cast<uint4 *>(a.codes + row * (J >> 1) + (blk << 4)) = codes;
   a.scales[scale_offset(a.scale_layout, row, blk, J)] = static_cast<uint8_t>(byte);
 }
 
-__global__ void __launch_bounds__(256, 3) quant_rows_kernel(QuantArgs a) {
+// Blocks ba and bb (bb == ba: one block).
+__device__ __forceinline__ void quant_rows_pair(const QuantArgs &a, int64_t ba, const uint4 (&ra)[4], int64_t bb,
+                                                const uint4 (&rb)[4]) {
+  uint64_t p[32];
+  {
+    float xa[32], xb[32];
+    load_row_block(a, ba, ra, xa);
+    load_row_block(a, bb, rb, xb);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) p[i] = pack2(xa[i], xb[i]);
+  }
+  uint4 ca, cb;
+  uint32_t ya, yb;
+  quantize32x2(p, a.hadamard, ca, cb, ya, yb);
+  store_row_block(a, ba, ca, ya);
+  if (bb != ba) store_row_block(a, bb, cb, yb);
+}
+
+__global__ void __launch_bounds__(256, 2) quant_rows_kernel(QuantArgs a) {
   const int64_t total = a.rows * (a.cols >> 5);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -216,66 +323,86 @@ __global__ void __launch_bounds__(256, 3) quant_rows_kernel(QuantArgs a) {
     for (int k = 0; k < 4; ++k) r0[k] = __ldg(src + 4 * b + k);
 #pragma unroll
     for (int k = 0; k < 4; ++k) r1[k] = __ldg(src + 4 * (b + stride) + k);
-    quant_rows_block(a, b, r0);
-    quant_rows_block(a, b + stride, r1);
+    quant_rows_pair(a, b, r0, b + stride, r1);
   }
   if (b < total) {
     uint4 r0[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) r0[k] = __ldg(src + 4 * b + k);
-    quant_rows_block(a, b, r0);
+    quant_rows_pair(a, b, r0, b, r0);
   }
 }
 
 // ---------------------------------------------------------------------------------------------
-// cols kernel: lines = columns of T, J = rows.  Tile 64 rows x 128 cols, 128 threads; thread t
-// takes the column pair (2 (t % 64), 2 (t % 64) + 1) and the 32-row block t / 64.  Small tiles
-// let six CTAs share an SM, so that some load while others compute.
+// Shared by the cols and dual kernels: a 64 x 128 tile of bf16 pairs in shared memory, and the
+// column-orientation pass over it (J = rows): thread t takes the column pair
+// (2 (t % 64), 2 (t % 64) + 1) and the 32-row block t / 64, both columns side by side.  Small
+// tiles let six CTAs share an SM, so that some load while others compute.
 // ---------------------------------------------------------------------------------------------
 constexpr int kColTile = 128;                     // columns per tile
 constexpr int kTileRows = 64;                     // rows per tile (two 32-row blocks)
 constexpr int kTileThreads = 128;
 
-__global__ void __launch_bounds__(kTileThreads, 6) quant_cols_kernel(QuantArgs a) {
-  __shared__ __align__(16) uint32_t tile[kTileRows][kColTile / 2];   // bf16 pairs
-  const int64_t R = a.rows, C = a.cols;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTileRows;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kColTile;
+template <int PITCH>
+__device__ __forceinline__ void load_tile(const QuantArgs &a, int64_t r0, int64_t c0, uint32_t (*tile)[PITCH]) {
   const int tid = threadIdx.x;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {                   // 1024 chunks of 16 B, 16 per tile row
     const int chunk = tid + kTileThreads * k;
     const int row = chunk >> 4, cc = (chunk & 15) << 2;   // cc in 32-bit words
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * C + c0) + (chunk & 15));
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * a.cols + c0) + (chunk & 15));
     *reinterpret_cast<uint4 *>(&tile[row][cc]) = v;
   }
-  __syncthreads();
+}
+
+template <int PITCH>
+__device__ __forceinline__ void quant_tile_cols(const QuantArgs &a, int64_t r0, int64_t c0, const uint32_t (*tile)[PITCH],
+                                                uint8_t *codes, uint8_t *scales) {
+  const int64_t R = a.rows;
+  const int tid = threadIdx.x;
   const int cp = tid & 63;                        // column pair
   const int rb = tid >> 6;                        // 32-row block inside the tile
   const int64_t blk = (r0 >> 5) + rb;
+  const int64_t line0 = c0 + 2 * cp;
   uint32_t zr = 0;
   if (a.zero_rows) zr = a.zero_rows[(r0 + 32 * rb) >> 5];
-#pragma unroll 1
-  for (int h = 0; h < 2; ++h) {                   // the two columns of the pair, one at a time
-    const int64_t line = c0 + 2 * cp + h;
-    uint32_t zmask = zr;
-    if (a.zero_cols && ((a.zero_cols[line >> 5] >> (line & 31)) & 1u)) zmask = 0xFFFFFFFFu;
-    float x[32];
+  uint32_t z0 = zr, z1 = zr;
+  if (a.zero_cols) {
+    const uint32_t zc = a.zero_cols[line0 >> 5];
+    if ((zc >> (line0 & 31)) & 1u) z0 = 0xFFFFFFFFu;
+    if ((zc >> ((line0 + 1) & 31)) & 1u) z1 = 0xFFFFFFFFu;
+  }
+  uint64_t p[32];
+  {
+    float x0[32], x1[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const uint32_t w = tile[32 * rb + i][cp];
-      x[i] = bf16_bits_to_f32(h ? (w >> 16) : (w & 0xFFFFu));
+      x0[i] = bf16_bits_to_f32(w & 0xFFFFu);
+      x1[i] = bf16_bits_to_f32(w >> 16);
     }
-    if (zmask) {
+    apply_zero_mask(x0, z0);
+    apply_zero_mask(x1, z1);
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if ((zmask >> i) & 1u) x[i] = 0.0f;
-    }
-    uint4 codes;
-    const uint32_t byte = quantize32(x, a.hadamard, codes);
-    *reinterpret_cast<uint4 *>(a.codes + line * (R >> 1) + (blk << 4)) = codes;
-    a.scales[scale_offset(a.scale_layout, line, blk, R)] = static_cast<uint8_t>(byte);
+    for (int i = 0; i < 32; ++i) p[i] = pack2(x0[i], x1[i]);
   }
+  uint4 c0c, c1c;
+  uint32_t y0, y1;
+  quantize32x2(p, a.hadamard, c0c, c1c, y0, y1);
+  *reinterpret_cast<uint4 *>(codes + line0 * (R >> 1) + (blk << 4)) = c0c;
+  *reinterpret_cast<uint4 *>(codes + (line0 + 1) * (R >> 1) + (blk << 4)) = c1c;
+  scales[scale_offset(a.scale_layout, line0, blk, R)] = static_cast<uint8_t>(y0);
+  scales[scale_offset(a.scale_layout, line0 + 1, blk, R)] = static_cast<uint8_t>(y1);
+}
+
+// cols kernel: lines = columns of T, J = rows.
+__global__ void __launch_bounds__(kTileThreads, 6) quant_cols_kernel(QuantArgs a) {
+  __shared__ __align__(16) uint32_t tile[kTileRows][kColTile / 2];   // bf16 pairs
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTileRows;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kColTile;
+  load_tile<kColTile / 2>(a, r0, c0, tile);
+  __syncthreads();
+  quant_tile_cols<kColTile / 2>(a, r0, c0, tile, a.codes, a.scales);
 }
 
 // ---------------------------------------------------------------------------------------------
