@@ -574,6 +574,56 @@ def profile(q, device, args):
         print(f"profiled one step: {b.launches_per_step()} launches")
         return
     from synthetic import normal_bf16
+    if args.profile == "foid":
+        M, N, r = 32768, 14336, 64                      # row probe of the gate G_Y (dgrad / wgrad OE)
+        G = normal_bf16(M, N, 1e-3, 3, outlier_axis="row", outlier_count=64, outlier_scale=40.0, device=device)
+        idx = torch.empty(r, dtype=torch.int32, device=device)
+        mask = torch.empty((M + 31) // 32, dtype=torch.int32, device=device)
+        ws = q.new_workspace(q.adahop_foid_workspace_size(M, r), device=device)
+        for _ in range(3):
+            q.adahop_foid(G, 0, r, idx, mask, ws)
+        torch.cuda.synchronize()
+        print("profiled 3 FOID calls (local + merge)")
+        return
+    if args.profile == "scatter":
+        P, Q, r, S = 32768, 4096, 64, 4                 # dgrad outer OE of the gate projection
+        C = torch.zeros((P, Q), dtype=torch.bfloat16, device=device)
+        part = torch.randn((S, r, Q), device=device)
+        idx = torch.randperm(P, device=device)[:r].sort().values.to(torch.int32)
+        for _ in range(3):
+            q.adahop_scatter_add(C, part, S, idx, r, 0)
+        torch.cuda.synchronize()
+        print("profiled 3 scatter-add launches")
+        return
+    if args.profile in ("bf16", "outlier"):
+        ws = q.new_workspace(4096, device=device)
+        if args.profile == "bf16":                      # BF16 strategy / baseline: q projection fwd
+            P, Q, J, S = 32768, 4096, 4096, 1
+        else:                                           # outer-OE outlier GEMM: 64 rows x W (gate dgrad)
+            P, Q, J, S = 64, 4096, 14336, 8
+        A = normal_bf16(P, J, 1.0, 1, device=device)
+        # fwd: B^T = W stored Q x J (K-major); outlier GEMM: B = W stored J x Q (MN-major), as dgrad reads it
+        b_kmajor = 1 if args.profile == "bf16" else 0
+        B = normal_bf16(Q, J, 0.02, 2, device=device) if b_kmajor else normal_bf16(J, Q, 0.02, 2, device=device)
+        C = torch.empty((P, Q), dtype=torch.bfloat16, device=device) if S == 1 else None
+        part = torch.empty((S, P, Q), dtype=torch.float32, device=device) if S > 1 else None
+        for _ in range(3):
+            q.adahop_gemm_bf16(A, 1, B, b_kmajor, P, Q, J, C, ws, splits=S, c_partial=part)
+        torch.cuda.synchronize()
+        assert q.adahop_get_device_status(ws) == 0
+        print(f"profiled 3 BF16 GEMM launches ({P} x {Q} x {J}, splits {S})")
+        return
+    if args.profile == "quant1":
+        M, N = 32768, 14336
+        G = normal_bf16(M, N, 1e-3, 3, device=device)
+        c = torch.empty(M * N // 2, dtype=torch.uint8, device=device)
+        sf = torch.empty(M * N // 32, dtype=torch.uint8, device=device)
+        for axis in (1, 0):
+            for _ in range(3):
+                q.adahop_quantize_mxfp4(G, axis, 1, None, None, c, sf, 1)
+        torch.cuda.synchronize()
+        print("profiled 3 rows + 3 cols quantiser launches")
+        return
     if args.profile == "quant":
         M, N = 32768, 14336                             # G_Y of the gate projection
         G = normal_bf16(M, N, 1e-3, 3, device=device)
@@ -615,11 +665,16 @@ def main():
     ap.add_argument("--sweep-m", default=None, help="comma-separated M values for --sweep")
     ap.add_argument("--quality", action="store_true",
                     help="relative MSE of the Table 3 plans on the 8B gate projection; prints one JSON object")
-    ap.add_argument("--profile", choices=["step", "gemm", "quant"], default=None,
+    ap.add_argument("--profile", choices=["step", "gemm", "quant", "quant1", "foid", "scatter", "bf16", "outlier"],
+                    default=None,
                     help="for ncu only (prints no bench line): 'step' = warm-up steps then one step "
                          "of the workload; 'gemm' = three launches of the fused MXFP4 GEMM on the "
                          "dgrad shape P=32768, Q=4096, J=14336; 'quant' = three launches of the "
-                         "dual-orientation quantiser on the 32768 x 14336 G_Y")
+                         "dual-orientation quantiser on the 32768 x 14336 G_Y; 'quant1' = three rows- "
+                         "and three cols-orientation launches on it; 'foid' = three row FOID calls on it "
+                         "(r = 64); 'scatter' = three scatter-adds of 64 rows into 32768 x 4096; 'bf16' = "
+                         "three BF16 GEMMs 32768 x 4096 x 4096; 'outlier' = three split-K BF16 GEMMs "
+                         "64 x 4096 x 14336 (8 splits)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
