@@ -11,11 +11,13 @@
 // equal variance the lower index first.  Keys are unique, so the top-r set is well defined.
 //
 // Stage 1 (grid): each CTA scores one chunk of 256..2048 lines (the smallest chunk that keeps
-// at most 8192 candidates overall), sorts their keys in shared memory (bitonic) and writes its
-// best r.  Stage 2 (one CTA): reduces the sorted runs pairwise -- the element-wise maximum of a
-// run and the reverse of its partner is a bitonic sequence holding exactly their best keys, which
-// half-cleaner steps sort again -- then writes the best r indices in ascending order and the
-// bitmap of selected lines.
+// at most 8192 candidates overall); every warp sorts 32 keys in registers (bitonic network over
+// shuffles), then merge levels in shared memory keep the best r of each merged pair until one
+// run remains, written out as the chunk's r candidates.  Stage 2 (one CTA): merge levels over
+// the chunks' runs down to the global best r, then each selected line's position in ascending
+// line order is its count of smaller selected lines.  A merge level is one pass: output i of the
+// best keys of sorted runs A and B is max(A[a], B[i - a]), where a, the number of A's keys among
+// the i best, comes from a binary search (A[m] belongs to the i best iff A[m] > B[i - m - 1]).
 #include <mutex>
 
 #include "common.cuh"
@@ -29,7 +31,8 @@ constexpr int kFoidThreads = 512;
 constexpr int kFoidMaxChunk = 2048;         // lines per stage-1 CTA, at most
 constexpr int kFoidMinChunk = 256;
 constexpr int kFoidMergeMaxKeys = 8192;     // candidates written by stage 1, at most
-constexpr int kFoidMergeSmemKeys = 16384;   // stage-2 shared memory (runs padded to a power of 2)
+// stage-2 shared memory: the candidates plus the first level's output (at most half of them + r)
+constexpr int kFoidMergeSmemKeys = kFoidMergeMaxKeys + kFoidMergeMaxKeys / 2 + 256;
 
 int pow2_at_least(int v) {
   int p = 1;
@@ -94,121 +97,112 @@ __device__ __forceinline__ uint64_t foid_key(const uint16_t *__restrict__ T, int
          static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(line));
 }
 
-// In-place bitonic sort of n (power of two) keys in shared memory, descending.
-__device__ void bitonic_sort_desc(uint64_t *keys, int n) {
-  for (int k = 2; k <= n; k <<= 1) {
+// Sorts the warp's 32 keys (one per lane) descending across the lanes: lane i ends with the
+// (i+1)-th largest.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t key) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint64_t a = keys[i], b = keys[ixj];
-          const bool up = (i & k) == 0;     // this run ends descending
-          if (up ? (a < b) : (a > b)) {
-            keys[i] = b;
-            keys[ixj] = a;
-          }
-        }
-      }
-      __syncthreads();
+      const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, key, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      key = keep_max ? (key > other ? key : other) : (key < other ? key : other);
     }
   }
+  return key;
+}
+
+// The (i+1)-th largest key of the union of A[0..la) and B[0..lb), both sorted descending, keys
+// distinct, i < la + lb.
+__device__ __forceinline__ uint64_t merge_at(const uint64_t *A, int la, const uint64_t *B, int lb, int i) {
+  int lo = i - lb > 0 ? i - lb : 0;
+  int hi = i < la ? i : la;
+  while (lo < hi) {                          // a = number of A's keys among the i largest
+    const int mid = (lo + hi) >> 1;
+    if (A[mid] > B[i - mid - 1])
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  const int b = i - lo;
+  if (lo >= la) return B[b];
+  if (b >= lb) return A[lo];
+  return A[lo] > B[b] ? A[lo] : B[b];
 }
 
 template <int AXIS>
 __global__ void __launch_bounds__(kFoidThreads) foid_local_kernel(const uint16_t *__restrict__ T,
                                                                   int64_t rows, int64_t cols, int r,
                                                                   int chunk, uint64_t *cand) {
-  __shared__ uint64_t keys[kFoidMaxChunk];
+  __shared__ uint64_t keys[2][kFoidMaxChunk];
   const int64_t lines = AXIS == 0 ? rows : cols;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * chunk;
-  for (int local = threadIdx.x; local < chunk; local += blockDim.x) {
-    const int64_t line = base + local;
-    keys[local] = line < lines ? foid_key<AXIS>(T, cols, line) : 0ull;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  for (int r0 = 32 * warp; r0 < chunk; r0 += 32 * nwarps) {
+    const int64_t line = base + r0 + lane;
+    const uint64_t key = line < lines ? foid_key<AXIS>(T, cols, line) : 0ull;
+    keys[0][r0 + lane] = warp_sort_desc(key);
   }
   __syncthreads();
-  bitonic_sort_desc(keys, chunk);
-  for (int i = threadIdx.x; i < r; i += blockDim.x) cand[static_cast<int64_t>(blockIdx.x) * r + i] = keys[i];
+  // chunk / 32 runs (a power of two) of equal length; keep the best min(2 len, r) of each pair
+  int g = chunk >> 5, len = 32, src = 0;
+  while (g > 1) {
+    const int out = 2 * len < r ? 2 * len : r;
+    const int pairs = g >> 1;
+    for (int o = tid; o < pairs * out; o += blockDim.x) {
+      const int p = o / out, i = o - p * out;
+      const uint64_t *A = keys[src] + 2 * p * len;
+      keys[src ^ 1][p * out + i] = merge_at(A, len, A + len, len, i);
+    }
+    __syncthreads();
+    src ^= 1;
+    g = pairs;
+    len = out;
+  }
+  for (int i = tid; i < r; i += blockDim.x)
+    cand[static_cast<int64_t>(blockIdx.x) * r + i] = i < len ? keys[src][i] : 0ull;
 }
 
-// ncand = runs * r candidates (each run sorted descending); runs are padded to rp2 in shared memory.
-__global__ void __launch_bounds__(1024) foid_merge_kernel(const uint64_t *cand, int runs, int r, int rp2,
-                                                          int64_t lines, int32_t *idx_out, uint32_t *mask_out) {
+// runs x r candidates (each run sorted descending, r keys).
+__global__ void __launch_bounds__(1024) foid_merge_kernel(const uint64_t *cand, int runs, int r, int64_t lines,
+                                                          int32_t *idx_out, uint32_t *mask_out) {
   extern __shared__ uint64_t skeys[];
-  __shared__ uint32_t sidx[256];
-  const int n = runs * rp2;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int run = i / rp2, k = i - run * rp2;
-    skeys[i] = k < r ? cand[static_cast<int64_t>(run) * r + k] : 0ull;
-  }
+  __shared__ uint32_t sline[256];
+  uint64_t *src = skeys, *dst = skeys + static_cast<int64_t>(runs) * r;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < runs * r; i += blockDim.x) src[i] = cand[i];
   const int64_t words = (lines + 31) >> 5;
   if (mask_out) {
-    for (int64_t w = threadIdx.x; w < words; w += blockDim.x) mask_out[w] = 0u;
+    for (int64_t w = tid; w < words; w += blockDim.x) mask_out[w] = 0u;
   }
   __syncthreads();
   if (r == 0) return;
   int g = runs;
   while (g > 1) {
     const int pairs = g >> 1;
-    const int m = pairs * rp2;
-    // max(run 2p, reverse(run 2p+1)) -> run p, staged through registers (at most 16 per thread)
-    uint64_t tmp[kFoidMergeSmemKeys / 1024];
-    int cnt = 0;
-    for (int i = threadIdx.x; i < m; i += blockDim.x, ++cnt) {
-      const int pr = i / rp2, k = i - pr * rp2;
-      const uint64_t a = skeys[(2 * pr) * rp2 + k], b = skeys[(2 * pr + 1) * rp2 + (rp2 - 1 - k)];
-      tmp[cnt] = a > b ? a : b;
+    for (int o = tid; o < pairs * r; o += blockDim.x) {
+      const int p = o / r, i = o - p * r;
+      const uint64_t *A = src + static_cast<int64_t>(2 * p) * r;
+      dst[o] = merge_at(A, r, A + r, r, i);
     }
-    uint64_t odd[kFoidMergeSmemKeys / 1024];
-    int ocnt = 0;
     if (g & 1) {
-      for (int k = threadIdx.x; k < rp2; k += blockDim.x, ++ocnt) odd[ocnt] = skeys[(g - 1) * rp2 + k];
+      for (int i = tid; i < r; i += blockDim.x) dst[pairs * r + i] = src[(g - 1) * r + i];
     }
     __syncthreads();
-    cnt = 0;
-    for (int i = threadIdx.x; i < m; i += blockDim.x, ++cnt) skeys[i] = tmp[cnt];
-    ocnt = 0;
-    if (g & 1) {
-      for (int k = threadIdx.x; k < rp2; k += blockDim.x, ++ocnt) skeys[pairs * rp2 + k] = odd[ocnt];
-    }
-    __syncthreads();
-    // each merged run is bitonic: half-cleaner steps sort it descending
-    for (int j = rp2 >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < m; i += blockDim.x) {
-        if ((i & j) == 0) {
-          const uint64_t a = skeys[i], b = skeys[i + j];
-          if (a < b) {
-            skeys[i] = b;
-            skeys[i + j] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
+    uint64_t *t = src;
+    src = dst;
+    dst = t;
     g = pairs + (g & 1);
   }
-  // the best r lines, then ascending order (pad with 0xFFFFFFFF)
-  for (int i = threadIdx.x; i < rp2; i += blockDim.x)
-    sidx[i] = i < r ? 0xFFFFFFFFu - static_cast<uint32_t>(skeys[i] & 0xFFFFFFFFull) : 0xFFFFFFFFu;
+  // src[0..r) holds the best r keys; each line's rank among them in ascending line order
+  for (int i = tid; i < r; i += blockDim.x) sline[i] = 0xFFFFFFFFu - static_cast<uint32_t>(src[i] & 0xFFFFFFFFull);
   __syncthreads();
-  for (int k = 2; k <= rp2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < rp2; i += blockDim.x) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint32_t a = sidx[i], b = sidx[ixj];
-          const bool up = (i & k) == 0;   // ascending run
-          if (up ? (a > b) : (a < b)) {
-            sidx[i] = b;
-            sidx[ixj] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int i = threadIdx.x; i < r; i += blockDim.x) {
-    const uint32_t l = sidx[i];
-    idx_out[i] = static_cast<int32_t>(l);
+  for (int i = tid; i < r; i += blockDim.x) {
+    const uint32_t l = sline[i];
+    int pos = 0;
+    for (int j = 0; j < r; ++j) pos += sline[j] < l ? 1 : 0;
+    idx_out[pos] = static_cast<int32_t>(l);
     if (mask_out) atomicOr(mask_out + (l >> 5), 1u << (l & 31));
   }
 }
@@ -228,7 +222,6 @@ cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis,
   const int chunk = foid_chunk(lines, r);
   const int64_t chunks = (lines + chunk - 1) / chunk;
   if (chunks * r > kFoidMergeMaxKeys) return cudaErrorInvalidValue;
-  const int rp2 = pow2_at_least(r > 0 ? r : 1);
   uint64_t *cand = static_cast<uint64_t *>(scratch);
   if (r > 0) {
     const int threads = chunk < kFoidThreads ? chunk : kFoidThreads;
@@ -238,11 +231,11 @@ cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis,
       foid_local_kernel<1><<<static_cast<unsigned>(chunks), threads, 0, s>>>(T, rows, cols, r, chunk, cand);
   }
   const int runs = r > 0 ? static_cast<int>(chunks) : 0;
-  const size_t smem = static_cast<size_t>(runs > 0 ? runs * rp2 : 1) * sizeof(uint64_t);
+  const size_t smem = static_cast<size_t>(runs > 0 ? runs * r + (runs + 1) / 2 * r : 1) * sizeof(uint64_t);
   cudaError_t e = cudaFuncSetAttribute(foid_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kFoidMergeSmemKeys * static_cast<int>(sizeof(uint64_t)));
   if (e != cudaSuccess) return e;
-  foid_merge_kernel<<<1, 1024, smem, s>>>(cand, runs, r, rp2, lines, idx_out, mask_out);
+  foid_merge_kernel<<<1, 1024, smem, s>>>(cand, runs, r, lines, idx_out, mask_out);
   return cudaGetLastError();
 }
 

@@ -30,7 +30,7 @@ cudaError_t launch_quant(const QuantArgs &a, int inner_axis, int num_sms, cudaSt
 // codes_cols / scales_cols the J = rows orientation (lines = cols); same masks and Hadamard flag.
 cudaError_t launch_quant_dual(const QuantArgs &a, uint8_t *codes_cols, uint8_t *scales_cols, cudaStream_t s);
 
-// FOID: stage 1 (per 2048-line chunk top-r) + stage 2 (merge, ascending indices, bitmap).
+// FOID: stage 1 (per-chunk top-r of 256..2048 lines) + stage 2 (merge, ascending indices, bitmap).
 size_t foid_scratch_bytes(int64_t lines, int r);
 cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
                         int32_t *idx_out, uint32_t *mask_out, void *scratch, cudaStream_t s);
