@@ -186,49 +186,58 @@ __device__ __forceinline__ void apply_zero_mask(float (&x)[32], uint32_t zmask) 
   }
 }
 
-// Quantises one 32-block held in registers (x[i] = element i, zeroed lines already +0):
-// optional orthonormal block-32 Sylvester Hadamard (butterflies with stride 1, 2, 4, 8, 16, each
-// (a, b) -> (a + b, a - b) rounded to float32, then * c), E8M0 scale from the block amax, E2M1
-// codes.  Returns the scale byte and writes 16 code bytes (element i in nibble i).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// bf16 pair word -> packed (low element, high element) as float32.
+__device__ __forceinline__ uint64_t unpack_bf16x2(uint32_t w) {
+  return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Quantises one 32-block held as 16 packed registers of adjacent elements, p[j] = (x_{2j},
+// x_{2j+1}) (zeroed lines already +0) -- the order of a row of bf16 pairs, so unpacking and the
+// final E2M1 conversion need no register shuffling.  Optional orthonormal block-32 Sylvester
+// Hadamard: the stride-1 butterflies are the two lanes of each register (scalar), strides
+// 2, 4, 8, 16 pair p[j] with p[j + h/2] two lanes at a time; every lane sees the same operands in
+// the same order as the scalar definition, so the results are identical.  Then E8M0 scale from
+// the block amax and E2M1 codes; returns the scale byte and writes 16 code bytes (element i in
+// nibble i).  An all-zero block gives byte 0 and codes 0.
 //
-// The block lives in 16 packed registers p[k] = (x_k, x_{k+16}): the stride 1..8 butterflies
-// pair p[k] with p[k + h] and run two at a time; stride 16 pairs the two lanes of p[k].  Every
-// lane sees the same operands in the same order as the scalar definition, so the results are
-// identical.  Scaling: with y the transformed block, the definition computes
-// v = RN(RN(y c) s), s = 2^(127 - byte), and amax = max |RN(y c)| = RN(max |y| c) (rounding is
-// monotonic and odd).  Where 2^-100 <= amax <= 2^100, c s is an exact normal float32 and
-// RN(y (c s)) equals RN(RN(y c) s) for every y with |y c| >= 2^-126 (power-of-two scaling of
-// normal floats is exact and commutes with rounding); smaller |y c| give |v| <= 2^-24 either way,
-// i.e. a signed zero code.  So one multiply replaces two there; elsewhere both are done.
-__device__ __forceinline__ uint32_t quantize32(const float (&x)[32], int hadamard, uint4 &codes) {
-  uint64_t p[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) p[k] = pack2(x[k], x[k + 16]);
+// Scaling: with y the transformed block, the definition computes v = RN(RN(y c) s),
+// s = 2^(127 - byte), and amax = max |RN(y c)| = RN(max |y| c) (rounding is monotonic and odd).
+// Where 2^-100 <= amax <= 2^100, c s is an exact normal float32 and RN(y (c s)) equals
+// RN(RN(y c) s) for every y with |y c| >= 2^-126 (power-of-two scaling of normal floats is
+// exact and commutes with rounding); smaller |y c| give |v| <= 2^-24 either way, i.e. a signed
+// zero code.  So one multiply replaces two there; elsewhere both are done.
+__device__ __forceinline__ uint32_t quantize32(uint64_t (&p)[16], int hadamard, uint4 &codes) {
   if (hadamard) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float lo, hi;
+      unpack2(p[j], lo, hi);
+      p[j] = pack2(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
+    }
 #pragma unroll
     for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if ((k & h) == 0) {
-          const uint64_t a = p[k], b = p[k + h];
-          p[k] = add2(a, b);
-          p[k + h] = sub2(a, b);
+      for (int j = 0; j < 16; ++j) {
+        if ((j & h) == 0) {
+          const uint64_t u = p[j], w = p[j + h];
+          p[j] = add2(u, w);
+          p[j + h] = sub2(u, w);
         }
       }
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      float lo, hi;
-      unpack2(p[k], lo, hi);
-      p[k] = pack2(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
     }
   }
   float amax = 0.0f;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
+  for (int j = 0; j < 16; ++j) {
     float lo, hi;
-    unpack2(p[k], lo, hi);
-    amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+    unpack2(p[j], lo, hi);
+    amax = max3(amax, fabsf(lo), fabsf(hi));
   }
   const float c = inv_sqrt32();
   if (hadamard) amax = __fmul_rn(amax, c);
@@ -238,18 +247,17 @@ __device__ __forceinline__ uint32_t quantize32(const float (&x)[32], int hadamar
     return byte;
   }
   const float s = mx_inv_scale(byte);
-  if (hadamard && !(amax >= 0x1p-100f && amax <= 0x1p100f)) {
+  const bool fast = amax >= 0x1p-100f && amax <= 0x1p100f;
+  if (hadamard && !fast) {
     const uint64_t cc = pack2(c, c);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) p[k] = mul2(p[k], cc);
+    for (int j = 0; j < 16; ++j) p[j] = mul2(p[j], cc);
   }
-  const float m = (hadamard && amax >= 0x1p-100f && amax <= 0x1p100f) ? __fmul_rn(c, s) : s;
+  const float m = (hadamard && fast) ? __fmul_rn(c, s) : s;
   const uint64_t mm = pack2(m, m);
-#pragma unroll
-  for (int k = 0; k < 16; ++k) p[k] = mul2(p[k], mm);
   float v[32];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) unpack2(p[k], v[k], v[k + 16]);
+  for (int j = 0; j < 16; ++j) unpack2(mul2(p[j], mm), v[2 * j], v[2 * j + 1]);
   codes.x = e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
   codes.y = e2m1x8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
   codes.z = e2m1x8(v[16], v[17], v[18], v[19], v[20], v[21], v[22], v[23]);
@@ -439,24 +447,25 @@ __global__ void __launch_bounds__(kTileThreads, 6) quant_dual_kernel(QuantArgs a
       const int64_t blk = (c0 >> 5) + bl;
       uint32_t zmask = zrow ? 0xFFFFFFFFu : 0u;
       if (a.zero_cols) zmask |= a.zero_cols[blk];
-      float x[32];
+      uint32_t u[16];
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         const uint4 v = *reinterpret_cast<const uint4 *>(&tile[rr][16 * bl + 4 * w]);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          x[8 * w + 2 * j] = bf16_bits_to_f32(u[j] & 0xFFFFu);
-          x[8 * w + 2 * j + 1] = bf16_bits_to_f32(u[j] >> 16);
-        }
+        u[4 * w] = v.x;
+        u[4 * w + 1] = v.y;
+        u[4 * w + 2] = v.z;
+        u[4 * w + 3] = v.w;
       }
-      if (zmask) {
+      if (zmask) {                                    // word j holds elements 2j (low) and 2j + 1
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if ((zmask >> i) & 1u) x[i] = 0.0f;
+        for (int j = 0; j < 16; ++j)
+          u[j] &= ~((((zmask >> (2 * j)) & 1u) ? 0xFFFFu : 0u) | (((zmask >> (2 * j + 1)) & 1u) ? 0xFFFF0000u : 0u));
       }
+      uint64_t p[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) p[j] = unpack_bf16x2(u[j]);
       uint4 codes;
-      const uint32_t byte = quantize32(x, a.hadamard, codes);
+      const uint32_t byte = quantize32(p, a.hadamard, codes);
       *reinterpret_cast<uint4 *>(a.codes + row * (C >> 1) + (blk << 4)) = codes;
       a.scales[scale_offset(a.scale_layout, row, blk, C)] = static_cast<uint8_t>(byte);
     }
@@ -473,19 +482,18 @@ __global__ void __launch_bounds__(kTileThreads, 6) quant_dual_kernel(QuantArgs a
       const int64_t line = c0 + 2 * cp + h;
       uint32_t zmask = zr;
       if (a.zero_cols && ((a.zero_cols[line >> 5] >> (line & 31)) & 1u)) zmask = 0xFFFFFFFFu;
-      float x[32];
+      const uint32_t half = h ? 0xFFFF0000u : 0x0000FFFFu;   // this column's half of each word
+      uint64_t p[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t w = tile[32 * rb + i][cp];
-        x[i] = bf16_bits_to_f32(h ? (w >> 16) : (w & 0xFFFFu));
-      }
-      if (zmask) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if ((zmask >> i) & 1u) x[i] = 0.0f;
+      for (int j = 0; j < 16; ++j) {
+        uint32_t w0 = tile[32 * rb + 2 * j][cp], w1 = tile[32 * rb + 2 * j + 1][cp];
+        if ((zmask >> (2 * j)) & 1u) w0 &= ~half;
+        if ((zmask >> (2 * j + 1)) & 1u) w1 &= ~half;
+        p[j] = h ? pack2(__uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 & 0xFFFF0000u))
+                 : pack2(__uint_as_float(w0 << 16), __uint_as_float(w1 << 16));
       }
       uint4 codes;
-      const uint32_t byte = quantize32(x, a.hadamard, codes);
+      const uint32_t byte = quantize32(p, a.hadamard, codes);
       *reinterpret_cast<uint4 *>(codes_c + line * (R >> 1) + (blk << 4)) = codes;
       scales_c[scale_offset(a.scale_layout, line, blk, R)] = static_cast<uint8_t>(byte);
     }
