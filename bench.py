@@ -434,6 +434,8 @@ def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)          # before NCCL binds its communicator to a device
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
@@ -447,12 +449,20 @@ def barrier(world):
 
 
 def max_over_ranks(world, v: float) -> float:
+    """The largest v over all ranks (the slowest rank's time bounds the job)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(flops_per_step_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Weak scaling (every rank runs its own copy of the workload, no data-path collective):
+    the flops all ranks processed per step over the slowest rank's step time."""
+    return flops_per_step_per_rank * world / (ms_per_step / 1e3) / 1e12
 
 
 def run_reference(args, world, rank):
@@ -723,7 +733,7 @@ def main():
         raise SystemExit(f"device status {st} after the timed region")
 
     e2e_ms, h2d, d2h = b.e2e(steps=3, warmup=1)
-    value = b.flops_per_step * world / (ms / 1e3) / 1e12
+    value = whole_job_tflops(b.flops_per_step, world, ms)
 
     fp4_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * FP4_OVER_BF16
     achieved = gflops / gsec / 1e12
