@@ -41,6 +41,14 @@ WORKLOAD = "llama3.1-8b"
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor throughput on GB300
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 QUANT_BYTES_PER_ELEM = 2 + 0.5 + 1 / 32   # bf16 read + E2M1 write + E8M0 write
+MX_BYTES_PER_ELEM = 0.5 + 1 / 32             # one E2M1 code + its share of an E8M0 scale
+
+# DRAM traffic of the fused GEMM per launch, averaged over the 21 launches of one step, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/
+# gemm_mxf4_pair_step_traffic_llama3.1-8b.md).  It describes the kernel source it was taken on
+# (sha256 over the files below); for any other source the bench reports traffic as null.
+GEMM_SOURCES = ("quantized_gemm_foid_gb300/csrc/gemm.cu", "quantized_gemm_foid_gb300/csrc/common.cuh")
+GEMM_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
 
 
 # ------------------------------------------------------------------------------------ helpers
@@ -106,6 +114,23 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def gemm_source_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_traffic():
+    """Measured DRAM bytes per launch of the fused GEMM, or None when the kernel source has changed
+    since the counters were taken."""
+    if GEMM_TRAFFIC["source_sha256"] and GEMM_TRAFFIC["source_sha256"] == gemm_source_sha256():
+        return GEMM_TRAFFIC["bytes_per_launch"]
+    return None
 
 
 def cuda_time_ms(fn, reps: int, stream=None) -> float:
@@ -276,9 +301,11 @@ class Bench:
     def gemm_roofline(self, reps: int = 3):
         """Times the fused MXFP4 (+BF16 outlier) GEMM of every GEMM of one step on its own
         (operands quantised once beforehand), CUDA events on the launching stream.
-        Returns (flops, seconds) summed over the step's GEMMs."""
+        Returns (flops, seconds, per-GEMM records, algorithmic DRAM bytes) summed over the step's
+        GEMMs; the algorithmic bytes are the MXFP4 operands and BF16 outlier slices read once and
+        the bf16 output written once."""
         q = self.q
-        tot_flops, tot_s, per = 0, 0.0, []
+        tot_flops, tot_s, per, tot_bytes = 0, 0.0, [], 0
         for c in self.cases:
             p = c.plan
             for gemm, strat in (("fwd", p.fwd), ("dgrad", p.dgrad), ("wgrad", p.wgrad)):
@@ -308,10 +335,11 @@ class Bench:
                 f = 2 * P * Q * J + 2 * P * Q * r
                 tot_flops += f
                 tot_s += ms / 1e3
+                tot_bytes += (P + Q) * J * MX_BYTES_PER_ELEM + 2 * (P + Q) * r + 2 * P * Q
                 per.append({"linear": c.name, "gemm": gemm, "P": P, "Q": Q, "J": J, "r": r,
                             "ms": round(ms, 4), "tflops": round(f / ms / 1e9, 1)})
                 del ac, asf, bc, bsf, Ao, Bo
-        return tot_flops, tot_s, per
+        return tot_flops, tot_s, per, tot_bytes
 
     def prep_bandwidth(self, reps: int = 5):
         """Algorithmic-byte bandwidth of the IHT + MXFP4 quantiser on the largest operand
@@ -326,6 +354,15 @@ class Bench:
             ms = cuda_time_ms(lambda: q.adahop_quantize_mxfp4(c.GY, axis, 1, None, None, codes, sf, 1), reps)
             out[name] = {"ms": round(ms, 4), "gbs": round(n * QUANT_BYTES_PER_ELEM / ms / 1e6, 1),
                          "shape": [c.M, c.N]}
+        # both orientations from one read (the step's G_Y / X / W pass): 2 + 2 x 0.53 B per element
+        n = c.M * c.N
+        cr = torch.empty(n // 2, dtype=torch.uint8, device=self.device)
+        sr = torch.empty(n // 32, dtype=torch.uint8, device=self.device)
+        cc = torch.empty(n // 2, dtype=torch.uint8, device=self.device)
+        sc = torch.empty(n // 32, dtype=torch.uint8, device=self.device)
+        ms = cuda_time_ms(lambda: q.adahop_quantize_mxfp4_dual(c.GY, 1, None, None, cr, sr, cc, sc, 1), reps)
+        out["dual"] = {"ms": round(ms, 4), "gbs": round(n * (2 + 2 * MX_BYTES_PER_ELEM) / ms / 1e6, 1),
+                       "shape": [c.M, c.N]}
         return out
 
     # ------------------------------------------------------------------ end to end (host buffers)
@@ -724,7 +761,7 @@ def main():
     ms = cuda_time_ms(b.step, args.steps)
     barrier(world)
     ms = max_over_ranks(world, ms)
-    gflops, gsec, per_gemm = b.gemm_roofline()
+    gflops, gsec, per_gemm, gbytes = b.gemm_roofline()
     prep = b.prep_bandwidth()
     variants = b.variants()
     clocks = sampler.stop()
@@ -749,7 +786,8 @@ def main():
         "roofline": {"kernel": "fused MXFP4 + BF16-outlier tcgen05 GEMM", "bound": "tensor",
                      "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
                      "peak_source": f"{peak_kind}: bf16_tflops_sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
-                     "traffic": None, "launches": len(per_gemm)},
+                     "traffic": gemm_traffic(), "traffic_unit": "bytes per launch (DRAM, ncu)",
+                     "algorithmic_bytes": gbytes / max(1, len(per_gemm)), "launches": len(per_gemm)},
         "prep": {"kernel": "IHT + MXFP4 quantiser", "bound": "hbm", "peak_gbs": peaks.get("hbm_gbs"),
                  **{k: dict(v, frac=round(v["gbs"] / peaks.get("hbm_gbs", 6800.0), 3)) for k, v in prep.items()}},
         "variants": variants,

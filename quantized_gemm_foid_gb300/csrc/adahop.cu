@@ -278,6 +278,13 @@ adahop_status mxf4_gemm(const Ctx &cx, const uint8_t *ac, const uint8_t *asf, co
     maps.ao = maps.a;
     maps.bo = maps.b;
   }
+  // C is written by TMA stores of 32 rows x 32 bytes (16 bf16 or 8 fp32 columns), 32-byte swizzle
+  if (C) {
+    if (out_dtype == 1)
+      ST_TRY(make_map(&maps.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, Q, P, 8, 32, CU_TENSOR_MAP_SWIZZLE_32B));
+    else
+      ST_TRY(make_map(&maps.c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, Q, P, 16, 32, CU_TENSOR_MAP_SWIZZLE_32B));
+  }
   GemmArgs g{};
   g.P = P; g.Q = Q; g.J = J;
   g.kind = 0;

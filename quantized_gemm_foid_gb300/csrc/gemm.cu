@@ -27,7 +27,10 @@
 // epilogue (two warps per 32-lane quadrant, each draining 128 of the 256 accumulator columns).
 // Tensor memory holds the 128 x 256 float32 accumulator (columns 0..255) and per-stage scale
 // factors above it.  The epilogue copies the accumulator to registers and releases it before
-// storing, so the next tile's MMAs overlap the stores.  Every mbarrier wait is bounded
+// storing, so the next tile's MMAs overlap the stores.  In the MXFP4 kernel the stores go through
+// shared memory: each epilogue warp converts 32 rows x 32 bytes of C into a 1 KB swizzled box
+// and writes it with a TMA bulk store, which turns one-row-per-lane global stores into whole
+// box writes (the J = 1024 shapes are bound by this store stream).  Every mbarrier wait is bounded
 // (common.cuh); on expiry the kernel sets the status word, stops issuing work, drains what it
 // issued, frees tensor memory and returns.
 #include "common.cuh"
@@ -57,7 +60,13 @@ struct PairCfg {
   // bytes counted on the even CTA's stage barrier: both CTAs' loads (TMA counts whole boxes)
   static constexpr uint32_t kTxMain = 2 * kStageBytes;
   static constexpr uint32_t kTxTail = 2 * (kABytes + kBBytes);
+  // epilogue staging: per epilogue warp kEpiBufs buffers of 32 rows x 32 bytes (TMA store boxes)
+  static constexpr int kEpiBufs = 1;
+  static constexpr uint32_t kEpiBufBytes = 1024;
+  static constexpr uint32_t kEpiOffset = kStages * kStageBytes;
+  static constexpr uint32_t kSmemBytes = kEpiOffset + kEpiWarps * kEpiBufs * kEpiBufBytes;
 };
+static_assert(PairCfg::kEpiOffset % 1024 == 0, "epilogue buffers need the swizzle alignment");
 static_assert(PairCfg::kStageBytes % 1024 == 0, "stage layout");
 static_assert(kSfTmemBase + PairCfg::kStages * PairCfg::kSfCols <= kTmemCols, "TMEM budget");
 
@@ -276,6 +285,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       constexpr uint32_t idesc_bf16 = make_idesc_bf16(C::kBM, BN, false, false);
+      // Scale factors of main-loop step `step` (in pipeline stage `stg`) -> tensor memory.
+      // SF-A atom ka -> columns sfa + 4 ka; SF-B rows 0..127 -> sfb + 8 ka, 128..255 -> +4.  The
+      // last slice of a J that is an odd multiple of 128 holds one scale atom (and two MMAs).
+      auto copy_scales = [&](int stg, int step) {
+        const uint32_t sA = smem_base + stg * C::kStageBytes;
+        const uint32_t sfa_t = tmem + kSfTmemBase + stg * C::kSfCols;
+        const uint32_t sfb_t = sfa_t + 8;
+        const bool half = (step == num_k - 1) && ((g.J & 255) != 0);
+#pragma unroll
+        for (int ka = 0; ka < 2; ++ka) {
+          if (ka == 1 && half) break;
+          tmem_cp_32x128b_x4_pair(sfa_t + 4 * ka, make_smem_desc(sA + C::kSFA + 512 * ka, 0, 128, kLayoutNone));
+          tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka, make_smem_desc(sA + C::kSFB + 512 * ka, 0, 128, kLayoutNone));
+          tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka + 4,
+                                  make_smem_desc(sA + C::kSFB + 1024 + 512 * ka, 0, 128, kLayoutNone));
+        }
+      };
       for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
         const int nsteps = num_k + tail;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.acc_empty), acc_phase ^ 1u, abort_flag))) {
@@ -295,20 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (step < num_k) {
               const uint32_t sfa_t = tmem + kSfTmemBase + stage * C::kSfCols;
               const uint32_t sfb_t = sfa_t + 8;
-              // the last slice of a J that is an odd multiple of 128 holds one scale atom and
-              // two MMAs
               const bool half = (step == num_k - 1) && ((g.J & 255) != 0);
-#pragma unroll
-              for (int ka = 0; ka < 2; ++ka) {
-                if (ka == 1 && half) break;
-                // SF-A atom ka -> columns sfa + 4 ka; SF-B rows 0..127 -> sfb + 8 ka, 128..255 -> +4
-                tmem_cp_32x128b_x4_pair(sfa_t + 4 * ka,
-                                        make_smem_desc(sA + C::kSFA + 512 * ka, 0, 128, kLayoutNone));
-                tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka,
-                                        make_smem_desc(sA + C::kSFB + 512 * ka, 0, 128, kLayoutNone));
-                tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka + 4,
-                                        make_smem_desc(sA + C::kSFB + 1024 + 512 * ka, 0, 128, kLayoutNone));
-              }
+              copy_scales(stage, step);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 if (kk == 2 && half) break;
@@ -358,7 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acc_empty = cluster_map(smem_u32(&ctl.acc_empty), 0);
     const bool can_store = g.C != nullptr;
     if (!can_store && threadIdx.x == 64) report_status(g.status, kStatusBadArg);
+    const uint32_t epi_buf = smem_base + C::kEpiOffset + static_cast<uint32_t>(warp - 2) * C::kEpiBufs * C::kEpiBufBytes;
+    uint32_t epi_seq = 0;
     uint32_t acc_phase = 0;
+    if (lane == 0 && can_store) prefetch_tensormap(&maps.c);
     for (int64_t tile = pair; tile < num_tiles; tile += num_pairs) {
       const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
       bool ready = true;
@@ -373,25 +390,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t v[4][32];
+      uint32_t v[128];                               // columns 128 half .. 128 half + 127 of this lane's row
       const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * quad) << 16) + 128u * half;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + 32u * j, v[j]);
+      for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + 32u * j, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * j));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty);
       acc_phase ^= 1u;
 
-      const int64_t row = t.m0 + 128 * rank + 32 * quad + lane;
-      if (can_store && row < g.P) {
+      // Stores through shared memory: each 32-row x 32-byte box (16 bf16 or 8 fp32 columns) is
+      // written by the warp into its staging buffer, lane i filling row i with the 32-byte swizzle
+      // (16-byte piece p at p ^ ((i >> 2) & 1): no bank conflicts), then stored by one TMA bulk
+      // copy that runs while the warp converts the next box.
+      const int32_t row0 = static_cast<int32_t>(t.m0 + 128 * rank + 32 * quad);   // 32 rows, all in or all out
+      if (can_store && row0 < g.P) {
+        const bool f32 = g.out_dtype == 1;
+        const int nbox = f32 ? 16 : 8;
+        const uint32_t sw = (static_cast<uint32_t>(lane) >> 2) & 1u;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int64_t col = t.n0 + 128 * half + 32 * j;
-          if (col < g.Q) store_row32(g, false, 0, row, col, v[j]);
+        for (int bx = 0; bx < 16; ++bx) {
+          if (bx >= nbox) break;
+          const int32_t col = static_cast<int32_t>(t.n0 + 128 * half) + (f32 ? 8 : 16) * bx;
+          if (col >= g.Q) break;                   // Q is a multiple of 128: whole boxes only
+          uint32_t w[2][4];
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            if (f32) {
+              const int e = 8 * bx + 4 * p;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) w[p][k] = v[e + k];
+            } else {
+              const int e = 16 * bx + 8 * p;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                w[p][k] = pack_bf16x2_rn(__uint_as_float(v[e + 2 * k]), __uint_as_float(v[e + 2 * k + 1]));
+            }
+          }
+          const uint32_t buf = epi_buf + (epi_seq % C::kEpiBufs) * C::kEpiBufBytes;
+          ++epi_seq;
+          if (lane == 0) bulk_wait_group_read<C::kEpiBufs - 1>();   // this buffer's last box has left it
+          __syncwarp();
+#pragma unroll
+          for (int p = 0; p < 2; ++p)
+            st_shared_v4(buf + 32u * lane + 16u * (static_cast<uint32_t>(p) ^ sw), w[p][0], w[p][1], w[p][2], w[p][3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&maps.c, buf, col, row0);
+            bulk_commit_group();
+          }
         }
       }
     }
+    if (lane == 0) bulk_wait_group<0>();             // staging buffers stay live until read
   }
 
   // neither CTA frees tensor memory or exits while its peer may still signal it
@@ -661,7 +714,7 @@ cudaError_t launch_bf16(const GemmArgs &g, const GemmMaps &maps, int num_sms, cu
 }  // namespace
 
 size_t gemm_smem_bytes(int kind) {
-  return kind == 0 ? PairCfg::kStages * PairCfg::kStageBytes + 1024
+  return kind == 0 ? PairCfg::kSmemBytes + 1024
                    : Bf16Cfg::kStages * Bf16Cfg::kStageBytes + 1024;
 }
 

@@ -64,9 +64,10 @@ struct GemmArgs {
 };
 // MXFP4: a / b are the E2M1 codes (128-byte rows, 128 rows per box), sfa / sfb the tensor-core
 // scale atoms viewed as rows of 128 uint32 (one 512-byte atom per row, two atoms per box), ao / bo
-// the BF16 outlier slices.  BF16: a / b only.
+// the BF16 outlier slices, c the output C (MXFP4 only: 32-row boxes of 32 bytes, 32-byte swizzle,
+// written by TMA stores; unused when C is null).  BF16: a / b only.
 struct GemmMaps {
-  CUtensorMap a, b, ao, bo, sfa, sfb;
+  CUtensorMap a, b, ao, bo, sfa, sfb, c;
 };
 cudaError_t launch_gemm(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s);
 size_t gemm_smem_bytes(int kind);

@@ -484,13 +484,22 @@ __global__ void __launch_bounds__(kTileThreads, 6) quant_dual_kernel(QuantArgs a
       if (a.zero_cols && ((a.zero_cols[line >> 5] >> (line & 31)) & 1u)) zmask = 0xFFFFFFFFu;
       const uint32_t half = h ? 0xFFFF0000u : 0x0000FFFFu;   // this column's half of each word
       uint64_t p[16];
+      if (zmask == 0u) {                                     // no zeroed rows or column: plain widening
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        uint32_t w0 = tile[32 * rb + 2 * j][cp], w1 = tile[32 * rb + 2 * j + 1][cp];
-        if ((zmask >> (2 * j)) & 1u) w0 &= ~half;
-        if ((zmask >> (2 * j + 1)) & 1u) w1 &= ~half;
-        p[j] = h ? pack2(__uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 & 0xFFFF0000u))
-                 : pack2(__uint_as_float(w0 << 16), __uint_as_float(w1 << 16));
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t w0 = tile[32 * rb + 2 * j][cp], w1 = tile[32 * rb + 2 * j + 1][cp];
+          p[j] = h ? pack2(__uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 & 0xFFFF0000u))
+                   : pack2(__uint_as_float(w0 << 16), __uint_as_float(w1 << 16));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          uint32_t w0 = tile[32 * rb + 2 * j][cp], w1 = tile[32 * rb + 2 * j + 1][cp];
+          if ((zmask >> (2 * j)) & 1u) w0 &= ~half;
+          if ((zmask >> (2 * j + 1)) & 1u) w1 &= ~half;
+          p[j] = h ? pack2(__uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 & 0xFFFF0000u))
+                   : pack2(__uint_as_float(w0 << 16), __uint_as_float(w1 << 16));
+        }
       }
       uint4 codes;
       const uint32_t byte = quantize32(p, a.hadamard, codes);
