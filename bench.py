@@ -272,6 +272,26 @@ class Bench:
                 "uniform_over_linears": all((c.plan.fwd, c.plan.dgrad, c.plan.wgrad) == (p.fwd, p.dgrad, p.wgrad)
                                             for c in self.cases)}
 
+    def graph_ms(self, steps: int = 10) -> float:
+        """One step captured in a CUDA graph (the C ABI is stream-ordered and allocates nothing,
+        so the 91 launches capture as they are), replayed `steps` times; CUDA events on the
+        replay stream.  Returns ms per step."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            self.step()                          # warm (per-device set-up happens outside capture)
+            s.synchronize()
+            with torch.cuda.graph(graph, stream=s):
+                self.step()
+        torch.cuda.synchronize()
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        ms = cuda_time_ms(graph.replay, steps)
+        del graph
+        return ms
+
     # ------------------------------------------------------------------ Table 3 variants
     def variants(self, steps: int = 5):
         """The same step under the plans of the pages' Table 3 rows, on the same kernels: all-BF16
@@ -764,6 +784,7 @@ def main():
     gflops, gsec, per_gemm, gbytes = b.gemm_roofline()
     prep = b.prep_bandwidth()
     variants = b.variants()
+    g_ms = b.graph_ms()
     clocks = sampler.stop()
     st = q.adahop_get_device_status(b.ws)
     if st != 0:
@@ -791,6 +812,8 @@ def main():
         "prep": {"kernel": "IHT + MXFP4 quantiser", "bound": "hbm", "peak_gbs": peaks.get("hbm_gbs"),
                  **{k: dict(v, frac=round(v["gbs"] / peaks.get("hbm_gbs", 6800.0), 3)) for k, v in prep.items()}},
         "variants": variants,
+        "cuda_graph": {"ms_per_step": g_ms, "value": b.flops_per_step / (g_ms / 1e3) / 1e12,
+                       "note": "the same step captured once in a CUDA graph and replayed"},
         "gemms": per_gemm,
         "clocks": clocks,
         "e2e": {"value": b.flops_per_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
