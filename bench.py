@@ -48,7 +48,8 @@ MX_BYTES_PER_ELEM = 0.5 + 1 / 32             # one E2M1 code + its share of an E
 # gemm_mxf4_pair_step_traffic_llama3.1-8b.md).  It describes the kernel source it was taken on
 # (sha256 over the files below); for any other source the bench reports traffic as null.
 GEMM_SOURCES = ("quantized_gemm_foid_gb300/csrc/gemm.cu", "quantized_gemm_foid_gb300/csrc/common.cuh")
-GEMM_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+GEMM_TRAFFIC = {"source_sha256": "7f260003419d37f30a188de8f69bfd6dcd44c0f774ce4031982a724cf813ac89",
+                "bytes_per_launch": 547208936}
 
 
 # ------------------------------------------------------------------------------------ helpers

@@ -285,23 +285,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       constexpr uint32_t idesc_bf16 = make_idesc_bf16(C::kBM, BN, false, false);
-      // Scale factors of main-loop step `step` (in pipeline stage `stg`) -> tensor memory.
-      // SF-A atom ka -> columns sfa + 4 ka; SF-B rows 0..127 -> sfb + 8 ka, 128..255 -> +4.  The
-      // last slice of a J that is an odd multiple of 128 holds one scale atom (and two MMAs).
-      auto copy_scales = [&](int stg, int step) {
-        const uint32_t sA = smem_base + stg * C::kStageBytes;
-        const uint32_t sfa_t = tmem + kSfTmemBase + stg * C::kSfCols;
-        const uint32_t sfb_t = sfa_t + 8;
-        const bool half = (step == num_k - 1) && ((g.J & 255) != 0);
-#pragma unroll
-        for (int ka = 0; ka < 2; ++ka) {
-          if (ka == 1 && half) break;
-          tmem_cp_32x128b_x4_pair(sfa_t + 4 * ka, make_smem_desc(sA + C::kSFA + 512 * ka, 0, 128, kLayoutNone));
-          tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka, make_smem_desc(sA + C::kSFB + 512 * ka, 0, 128, kLayoutNone));
-          tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka + 4,
-                                  make_smem_desc(sA + C::kSFB + 1024 + 512 * ka, 0, 128, kLayoutNone));
-        }
-      };
       for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
         const int nsteps = num_k + tail;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.acc_empty), acc_phase ^ 1u, abort_flag))) {
@@ -322,10 +305,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t sfa_t = tmem + kSfTmemBase + stage * C::kSfCols;
               const uint32_t sfb_t = sfa_t + 8;
               const bool half = (step == num_k - 1) && ((g.J & 255) != 0);
-              copy_scales(stage, step);
+              // Scale factors go to tensor memory just ahead of the two MMAs that read them (SF-A
+              // atom ka -> columns sfa + 4 ka; SF-B rows 0..127 -> sfb + 8 ka, 128..255 -> +4):
+              // interleaved with the MMAs, the copies cost the tensor pipe less than in one group.
+              // The last slice of a J that is an odd multiple of 128 holds one scale atom and two
+              // MMAs.
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 if (kk == 2 && half) break;
+                if ((kk & 1) == 0) {
+                  const int ka = kk >> 1;
+                  tmem_cp_32x128b_x4_pair(sfa_t + 4 * ka, make_smem_desc(sA + C::kSFA + 512 * ka, 0, 128, kLayoutNone));
+                  tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka, make_smem_desc(sA + C::kSFB + 512 * ka, 0, 128, kLayoutNone));
+                  tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka + 4,
+                                          make_smem_desc(sA + C::kSFB + 1024 + 512 * ka, 0, 128, kLayoutNone));
+                }
                 const uint64_t adesc = make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
                 const uint64_t bdesc = make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
                 constexpr uint32_t idesc0 = make_idesc_mxf4(C::kBM, BN, 0, 0);
