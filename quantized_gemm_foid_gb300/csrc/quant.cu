@@ -221,7 +221,7 @@ __device__ __forceinline__ uint32_t quantize32(uint64_t (&p)[16], int hadamard, 
       p[j] = pack2(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
     }
 #pragma unroll
-    for (int h = 1; h < 16; h <<= 1) {
+    for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         if ((j & h) == 0) {
@@ -233,11 +233,26 @@ __device__ __forceinline__ uint32_t quantize32(uint64_t (&p)[16], int hadamard, 
     }
   }
   float amax = 0.0f;
+  if (hadamard) {
+    // last stage (element stride 16); max(|u + w|, |u - w|) = |u| + |w| exactly, and rounding is
+    // monotonic and odd, so the block amax is the largest RN(|u| + |w|) over the pairs
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float lo, hi;
-    unpack2(p[j], lo, hi);
-    amax = max3(amax, fabsf(lo), fabsf(hi));
+    for (int j = 0; j < 8; ++j) {
+      const uint64_t u = p[j], w = p[j + 8];
+      float u0, u1, w0, w1;
+      unpack2(u, u0, u1);
+      unpack2(w, w0, w1);
+      amax = max3(amax, __fadd_rn(fabsf(u0), fabsf(w0)), __fadd_rn(fabsf(u1), fabsf(w1)));
+      p[j] = add2(u, w);
+      p[j + 8] = sub2(u, w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float lo, hi;
+      unpack2(p[j], lo, hi);
+      amax = max3(amax, fabsf(lo), fabsf(hi));
+    }
   }
   const float c = inv_sqrt32();
   if (hadamard) amax = __fmul_rn(amax, c);
