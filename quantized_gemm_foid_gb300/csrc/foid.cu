@@ -13,11 +13,12 @@
 // Stage 1 (grid): each CTA scores one chunk of 256..2048 lines (the smallest chunk that keeps
 // at most 8192 candidates overall); every warp sorts 32 keys in registers (bitonic network over
 // shuffles), then merge levels in shared memory keep the best r of each merged pair until one
-// run remains, written out as the chunk's r candidates.  Stage 2 (one CTA): merge levels over
-// the chunks' runs down to the global best r, then each selected line's position in ascending
-// line order is its count of smaller selected lines.  A merge level is one pass: output i of the
-// best keys of sorted runs A and B is max(A[a], B[i - a]), where a, the number of A's keys among
-// the i best, comes from a binary search (A[m] belongs to the i best iff A[m] > B[i - m - 1]).
+// run remains, written out as the chunk's r candidates.  A merge level is one pass: output i of
+// the best keys of sorted runs A and B is max(A[a], B[i - a]), where a, the number of A's keys
+// among the i best, comes from a binary search (A[m] belongs to the i best iff A[m] > B[i - m - 1]).
+// Stage 2 (one CTA): each warp holds a run of the best keys in its registers and folds the
+// chunks' runs into it with bitonic merges (shuffles, no shared-memory searches); a tree over the
+// warps leaves the global best r in one warp, which sorts their lines ascending.
 #include <mutex>
 
 #include "common.cuh"
@@ -31,8 +32,6 @@ constexpr int kFoidThreads = 512;
 constexpr int kFoidMaxChunk = 2048;         // lines per stage-1 CTA, at most
 constexpr int kFoidMinChunk = 256;
 constexpr int kFoidMergeMaxKeys = 8192;     // candidates written by stage 1, at most
-// stage-2 shared memory: the candidates plus the first level's output (at most half of them + r)
-constexpr int kFoidMergeSmemKeys = kFoidMergeMaxKeys + kFoidMergeMaxKeys / 2 + 256;
 
 int pow2_at_least(int v) {
   int p = 1;
@@ -164,46 +163,137 @@ __global__ void __launch_bounds__(kFoidThreads) foid_local_kernel(const uint16_t
     cand[static_cast<int64_t>(blockIdx.x) * r + i] = i < len ? keys[src][i] : 0ull;
 }
 
-// runs x r candidates (each run sorted descending, r keys).
-__global__ void __launch_bounds__(1024) foid_merge_kernel(const uint64_t *cand, int runs, int r, int64_t lines,
-                                                          int32_t *idx_out, uint32_t *mask_out) {
-  extern __shared__ uint64_t skeys[];
-  __shared__ uint32_t sline[256];
-  uint64_t *src = skeys, *dst = skeys + static_cast<int64_t>(runs) * r;
-  const int tid = threadIdx.x;
-  for (int i = tid; i < runs * r; i += blockDim.x) src[i] = cand[i];
+// ---------------------------------------------------------------------------------------------
+// Warp-held runs.  A run of R = 32 KPL keys sits in one warp, KPL registers per lane,
+// element e = 32 s + lane in register s, sorted descending.  Merging keeps the R largest of two
+// runs: with B reversed, max(A[e], B[R - 1 - e]) is a bitonic sequence holding exactly the R
+// largest keys of both (the first half-cleaner of a bitonic merge), and half-cleaners with
+// strides R/2, ..., 1 sort it -- strides of 32 and more between a lane's registers, smaller ones
+// across lanes by shuffles.  No shared-memory searches, no bank conflicts.
+// ---------------------------------------------------------------------------------------------
+constexpr int kMergeThreads = 512;            // 16 warps
+constexpr int kMergeWarps = kMergeThreads / 32;
+
+__device__ __forceinline__ uint64_t kmax(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ uint64_t kmin(uint64_t a, uint64_t b) { return a < b ? a : b; }
+
+template <int KPL>
+__device__ __forceinline__ void run_load(uint64_t (&k)[KPL], const uint64_t *src, int len, int lane) {
+#pragma unroll
+  for (int s = 0; s < KPL; ++s) {
+    const int e = 32 * s + lane;
+    k[s] = e < len ? src[e] : 0ull;           // 0 sorts below every real key
+  }
+}
+
+template <int KPL>
+__device__ __forceinline__ void run_merge(uint64_t (&a)[KPL], const uint64_t (&b)[KPL], int lane) {
+#pragma unroll
+  for (int s = 0; s < KPL; ++s) a[s] = kmax(a[s], __shfl_xor_sync(0xFFFFFFFFu, b[KPL - 1 - s], 31));
+#pragma unroll
+  for (int ks = KPL / 2; ks >= 1; ks >>= 1) {
+#pragma unroll
+    for (int s = 0; s < KPL; ++s) {
+      if ((s & ks) == 0) {
+        const uint64_t x = a[s], y = a[s | ks];
+        a[s] = kmax(x, y);
+        a[s | ks] = kmin(x, y);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 16; j >= 1; j >>= 1) {
+#pragma unroll
+    for (int s = 0; s < KPL; ++s) {
+      const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, a[s], j);
+      a[s] = (lane & j) == 0 ? kmax(a[s], o) : kmin(a[s], o);
+    }
+  }
+}
+
+// Sorts the warp's R = 32 KPL values ascending (full bitonic network over registers and lanes).
+template <int KPL>
+__device__ __forceinline__ void warp_sort_asc(uint32_t (&v)[KPL], int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32 * KPL; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 32) {
+        const int ks = stride >> 5;
+#pragma unroll
+        for (int s = 0; s < KPL; ++s) {
+          if ((s & ks) == 0) {
+            const bool up = ((32 * s + lane) & size) == 0;
+            const uint32_t x = v[s], y = v[s | ks];
+            v[s] = up ? min(x, y) : max(x, y);
+            v[s | ks] = up ? max(x, y) : min(x, y);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < KPL; ++s) {
+          const bool up = ((32 * s + lane) & size) == 0;
+          const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, v[s], stride);
+          v[s] = (((lane & stride) == 0) == up) ? min(v[s], o) : max(v[s], o);
+        }
+      }
+    }
+  }
+}
+
+// Stage 2: runs x r candidates (each run sorted descending, r keys).  Every warp folds its share
+// of the runs into one run of the R largest, a tree over the warps through shared memory leaves
+// the R largest in warp 0, whose first r are the selection; warp 0 then sorts their lines
+// ascending, writes them and sets their bits in the line bitmap (cleared first by all threads).
+template <int KPL>
+__global__ void __launch_bounds__(kMergeThreads) foid_merge_kernel(const uint64_t *cand, int runs, int r,
+                                                                   int64_t lines, int32_t *idx_out,
+                                                                   uint32_t *mask_out) {
+  __shared__ uint64_t sk[kMergeWarps][32 * KPL];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t words = (lines + 31) >> 5;
   if (mask_out) {
     for (int64_t w = tid; w < words; w += blockDim.x) mask_out[w] = 0u;
   }
-  __syncthreads();
   if (r == 0) return;
-  int g = runs;
-  while (g > 1) {
-    const int pairs = g >> 1;
-    for (int o = tid; o < pairs * r; o += blockDim.x) {
-      const int p = o / r, i = o - p * r;
-      const uint64_t *A = src + static_cast<int64_t>(2 * p) * r;
-      dst[o] = merge_at(A, r, A + r, r, i);
-    }
-    if (g & 1) {
-      for (int i = tid; i < r; i += blockDim.x) dst[pairs * r + i] = src[(g - 1) * r + i];
+  uint64_t top[KPL];
+#pragma unroll
+  for (int s = 0; s < KPL; ++s) top[s] = 0ull;
+  for (int run = warp; run < runs; run += kMergeWarps) {
+    uint64_t b[KPL];
+    run_load<KPL>(b, cand + static_cast<int64_t>(run) * r, r, lane);
+    run_merge<KPL>(top, b, lane);
+  }
+#pragma unroll
+  for (int s = 0; s < KPL; ++s) sk[warp][32 * s + lane] = top[s];
+  __syncthreads();                            // also orders the bitmap clearing before the bits below
+#pragma unroll
+  for (int half = kMergeWarps / 2; half >= 1; half >>= 1) {
+    if (warp < half) {
+      uint64_t b[KPL];
+      run_load<KPL>(b, sk[warp + half], 32 * KPL, lane);
+      run_merge<KPL>(top, b, lane);
+#pragma unroll
+      for (int s = 0; s < KPL; ++s) sk[warp][32 * s + lane] = top[s];
     }
     __syncthreads();
-    uint64_t *t = src;
-    src = dst;
-    dst = t;
-    g = pairs + (g & 1);
   }
-  // src[0..r) holds the best r keys; each line's rank among them in ascending line order
-  for (int i = tid; i < r; i += blockDim.x) sline[i] = 0xFFFFFFFFu - static_cast<uint32_t>(src[i] & 0xFFFFFFFFull);
-  __syncthreads();
-  for (int i = tid; i < r; i += blockDim.x) {
-    const uint32_t l = sline[i];
-    int pos = 0;
-    for (int j = 0; j < r; ++j) pos += sline[j] < l ? 1 : 0;
-    idx_out[pos] = static_cast<int32_t>(l);
-    if (mask_out) atomicOr(mask_out + (l >> 5), 1u << (l & 31));
+  if (warp == 0) {
+    uint32_t ln[KPL];
+#pragma unroll
+    for (int s = 0; s < KPL; ++s) {
+      const int e = 32 * s + lane;
+      ln[s] = e < r ? 0xFFFFFFFFu - static_cast<uint32_t>(top[s] & 0xFFFFFFFFull) : 0xFFFFFFFFu;
+    }
+    warp_sort_asc<KPL>(ln, lane);
+#pragma unroll
+    for (int s = 0; s < KPL; ++s) {
+      const int e = 32 * s + lane;
+      if (e < r) {
+        idx_out[e] = static_cast<int32_t>(ln[s]);
+        if (mask_out && ln[s] < lines) atomicOr(mask_out + (ln[s] >> 5), 1u << (ln[s] & 31));
+      }
+    }
   }
 }
 
@@ -231,11 +321,14 @@ cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis,
       foid_local_kernel<1><<<static_cast<unsigned>(chunks), threads, 0, s>>>(T, rows, cols, r, chunk, cand);
   }
   const int runs = r > 0 ? static_cast<int>(chunks) : 0;
-  const size_t smem = static_cast<size_t>(runs > 0 ? runs * r + (runs + 1) / 2 * r : 1) * sizeof(uint64_t);
-  cudaError_t e = cudaFuncSetAttribute(foid_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kFoidMergeSmemKeys * static_cast<int>(sizeof(uint64_t)));
-  if (e != cudaSuccess) return e;
-  foid_merge_kernel<<<1, 1024, smem, s>>>(cand, runs, r, lines, idx_out, mask_out);
+  if (r <= 32)
+    foid_merge_kernel<1><<<1, kMergeThreads, 0, s>>>(cand, runs, r, lines, idx_out, mask_out);
+  else if (r <= 64)
+    foid_merge_kernel<2><<<1, kMergeThreads, 0, s>>>(cand, runs, r, lines, idx_out, mask_out);
+  else if (r <= 128)
+    foid_merge_kernel<4><<<1, kMergeThreads, 0, s>>>(cand, runs, r, lines, idx_out, mask_out);
+  else
+    foid_merge_kernel<8><<<1, kMergeThreads, 0, s>>>(cand, runs, r, lines, idx_out, mask_out);
   return cudaGetLastError();
 }
 

@@ -431,13 +431,14 @@ __global__ void __launch_bounds__(kTileThreads, 6) quant_cols_kernel(QuantArgs a
 // ---------------------------------------------------------------------------------------------
 // dual kernel: both orientations of one tensor from a single read (prep fusion).  Tile 64 rows x
 // 128 cols staged in shared memory with 4-word row padding (conflict-free row reads and
-// column-pair reads), 128 threads, six CTAs per SM; each thread quantises two 32-blocks along the
-// tile's rows (J = cols) and one 32-row block of each column of a column pair (J = rows).  Same
-// arithmetic as the two kernels above.
+// column-pair reads), 128 threads, eight CTAs per SM (64 registers: the kernel is bound by
+// instruction issue, and more resident warps hide its latencies better than six did); each
+// thread quantises two 32-blocks along the tile's rows (J = cols) and one 32-row block of each
+// column of a column pair (J = rows).  Same arithmetic as the two kernels above.
 // ---------------------------------------------------------------------------------------------
 constexpr int kDualPitch = kColTile / 2 + 4;     // 32-bit words per staged row
 
-__global__ void __launch_bounds__(kTileThreads, 6) quant_dual_kernel(QuantArgs a, uint8_t *codes_c, uint8_t *scales_c) {
+__global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a, uint8_t *codes_c, uint8_t *scales_c) {
   __shared__ __align__(16) uint32_t tile[kTileRows][kDualPitch];
   const int64_t R = a.rows, C = a.cols;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTileRows;
