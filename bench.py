@@ -217,10 +217,10 @@ def launches_per_gemm(gemm: str, strategy: int, r: int, pats: dict, foid_shared:
 
 
 class Bench:
-    def __init__(self, q, device):
+    def __init__(self, q, device, wl=None):
         self.q = q
         self.device = device
-        self.wl = WORKLOADS[WORKLOAD]
+        self.wl = wl if wl is not None else WORKLOADS[WORKLOAD]
         self.cases = [LinearCase(q, self.wl, li, device) for li in range(len(self.wl.linears))]
         self.ws = q.new_workspace(max(c.ws_bytes(q) for c in self.cases), device=device)
         self.flops_per_step = sum(c.flops() for c in self.cases)
@@ -449,6 +449,30 @@ class Bench:
         return start.elapsed_time(end) / steps, h2d, d2h
 
 
+def host_link_gbs(device, nbytes: int = 1 << 30) -> dict:
+    """This box's pinned host <-> device copy bandwidth (best of three 1 GiB copies each way): the
+    bound the end-to-end number is read against."""
+    g = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    out = {}
+    for name in ("h2d", "d2h"):
+        best = None
+        for _ in range(3):
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record()
+            if name == "h2d":
+                g.copy_(h, non_blocking=True)
+            else:
+                h.copy_(g, non_blocking=True)
+            end.record()
+            torch.cuda.synchronize()
+            ms = start.elapsed_time(end)
+            best = ms if best is None else min(best, ms)
+        out[name] = round(nbytes / best / 1e6, 1)
+    del g, h
+    return out
+
+
 # ------------------------------------------------------------------------------------ CPU oracle
 def oracle_sample_step(cache: dict) -> tuple[float, int]:
     """One bounded sample of the workload through the CPU oracle: the first 256 tokens of the
@@ -587,6 +611,36 @@ def sweep(q, device, args):
                 del X, W, Y, ws
                 torch.cuda.empty_cache()
     print(json.dumps({"sweep": "llama3.1-8b down projection, Fwd", "K": K, "N": N, "points": points}))
+
+
+def batch_sweep(q, device, args):
+    """Throughput against batch size (the pages' Fig. 6 analogue): the Llama3.1-8B block's seven
+    linears, Fwd + dgrad + wgrad, at M = seq_len x batch tokens per step for seq_len 4096 and
+    batch 1..16, under the calibrated AdaHOP plan and under the all-BF16 plan on the same kernels.
+    CUDA events over 5 steps after 3 warm-up steps.  Prints one JSON object."""
+    import dataclasses
+    base = WORKLOADS[WORKLOAD]
+    points = []
+    for batch in (1, 2, 4, 8, 16):
+        M = 4096 * batch
+        b = Bench(q, device, wl=dataclasses.replace(base, M=M))
+        row = {"batch": batch, "tokens_per_step": M}
+        saved = [(c.plan.fwd, c.plan.dgrad, c.plan.wgrad) for c in b.cases]
+        for name, strat in (("adahop", None), ("bf16", 3)):
+            for c, orig in zip(b.cases, saved):
+                c.plan.fwd, c.plan.dgrad, c.plan.wgrad = orig if strat is None else (strat, strat, strat)
+            for _ in range(3):
+                b.step()
+            torch.cuda.synchronize()
+            ms = cuda_time_ms(b.step, 5)
+            assert q.adahop_get_device_status(b.ws) == 0
+            row[name] = {"ms_per_step": round(ms, 3), "tokens_per_s": round(M / ms * 1e3),
+                         "eff_tflops": round(b.flops_per_step / ms / 1e9, 1)}
+        row["speedup_vs_bf16"] = round(row["bf16"]["ms_per_step"] / row["adahop"]["ms_per_step"], 3)
+        points.append(row)
+        del b
+        torch.cuda.empty_cache()
+    print(json.dumps({"batch_sweep": "llama3.1-8b block linears fwd+bwd, seq_len 4096", "points": points}))
 
 
 def quality(q, device, args):
@@ -731,6 +785,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="OE rank / batch sweep (latency and relative MSE); prints one JSON object")
     ap.add_argument("--sweep-m", default=None, help="comma-separated M values for --sweep")
+    ap.add_argument("--batch-sweep", action="store_true",
+                    help="throughput against batch size (seq_len 4096, batch 1..16), AdaHOP and BF16 plans; "
+                         "prints one JSON object")
     ap.add_argument("--quality", action="store_true",
                     help="relative MSE of the Table 3 plans on the 8B gate projection; prints one JSON object")
     ap.add_argument("--profile", choices=["step", "gemm", "quant", "quant1", "foid", "scatter", "bf16", "outlier"],
@@ -763,6 +820,9 @@ def main():
     if args.quality:
         quality(q, device, args)
         return
+    if args.batch_sweep:
+        batch_sweep(q, device, args)
+        return
 
     peaks, peak_kind = load_peaks()
     b = Bench(q, device)
@@ -792,6 +852,7 @@ def main():
         raise SystemExit(f"device status {st} after the timed region")
 
     e2e_ms, h2d, d2h = b.e2e(steps=3, warmup=1)
+    link = host_link_gbs(device)
     value = whole_job_tflops(b.flops_per_step, world, ms)
 
     fp4_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * FP4_OVER_BF16
@@ -818,7 +879,9 @@ def main():
         "gemms": per_gemm,
         "clocks": clocks,
         "e2e": {"value": b.flops_per_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "host_link_gbs": link,
+                "copy_bound_ms_per_step": round(max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6, 2)},
         "gpu_launches": b.launches_per_step() * args.steps,
         # forward -> backward context per step: X in the wgrad orientation and W in the dgrad
         # orientation (MXFP4 codes + scales) against the bf16 copies of X a BF16 backward keeps

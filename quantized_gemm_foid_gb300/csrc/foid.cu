@@ -241,6 +241,50 @@ __device__ __forceinline__ void warp_sort_asc(uint32_t (&v)[KPL], int lane) {
   }
 }
 
+// Stage 1 for row probes: each warp scores 32 rows at a time, sorts them across its lanes and
+// folds them into the run of the R largest keys it holds; a tree over the warps through shared
+// memory leaves the chunk's R largest in warp 0, whose first r go to `cand`.  (Column probes use
+// foid_local_kernel<1>, whose strided probe loads leave no registers for the held runs.)
+template <int KPL>
+__global__ void __launch_bounds__(kFoidThreads, 1) foid_local_rows_kernel(const uint16_t *__restrict__ T,
+                                                                       int64_t rows, int64_t cols, int r,
+                                                                       int chunk, uint64_t *cand) {
+  __shared__ uint64_t sk[kFoidThreads / 32][32 * KPL];
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * chunk;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  uint64_t top[KPL];
+#pragma unroll
+  for (int s = 0; s < KPL; ++s) top[s] = 0ull;
+  for (int r0 = 32 * warp; r0 < chunk; r0 += 32 * nwarps) {
+    const int64_t line = base + r0 + lane;
+    uint64_t b[KPL];
+    b[0] = warp_sort_desc(line < rows ? foid_key<0>(T, cols, line) : 0ull);
+#pragma unroll
+    for (int s = 1; s < KPL; ++s) b[s] = 0ull;
+    run_merge<KPL>(top, b, lane);
+  }
+#pragma unroll
+  for (int s = 0; s < KPL; ++s) sk[warp][32 * s + lane] = top[s];
+  __syncthreads();
+  for (int half = nwarps / 2; half >= 1; half >>= 1) {
+    if (warp < half) {
+      uint64_t b[KPL];
+      run_load<KPL>(b, sk[warp + half], 32 * KPL, lane);
+      run_merge<KPL>(top, b, lane);
+#pragma unroll
+      for (int s = 0; s < KPL; ++s) sk[warp][32 * s + lane] = top[s];
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+#pragma unroll
+    for (int s = 0; s < KPL; ++s) {
+      const int e = 32 * s + lane;
+      if (e < r) cand[static_cast<int64_t>(blockIdx.x) * r + e] = top[s];
+    }
+  }
+}
+
 // Stage 2: runs x r candidates (each run sorted descending, r keys).  Every warp folds its share
 // of the runs into one run of the R largest, a tree over the warps through shared memory leaves
 // the R largest in warp 0, whose first r are the selection; warp 0 then sorts their lines
@@ -259,10 +303,21 @@ __global__ void __launch_bounds__(kMergeThreads) foid_merge_kernel(const uint64_
   uint64_t top[KPL];
 #pragma unroll
   for (int s = 0; s < KPL; ++s) top[s] = 0ull;
-  for (int run = warp; run < runs; run += kMergeWarps) {
-    uint64_t b[KPL];
-    run_load<KPL>(b, cand + static_cast<int64_t>(run) * r, r, lane);
-    run_merge<KPL>(top, b, lane);
+  // four runs' loads in flight per warp, then their merges
+  for (int run0 = warp; run0 < runs; run0 += 4 * kMergeWarps) {
+    uint64_t b[4][KPL];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int run = run0 + u * kMergeWarps;
+      if (run < runs) {
+        run_load<KPL>(b[u], cand + static_cast<int64_t>(run) * r, r, lane);
+      } else {
+#pragma unroll
+        for (int s = 0; s < KPL; ++s) b[u][s] = 0ull;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) run_merge<KPL>(top, b[u], lane);
   }
 #pragma unroll
   for (int s = 0; s < KPL; ++s) sk[warp][32 * s + lane] = top[s];
@@ -315,10 +370,17 @@ cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis,
   uint64_t *cand = static_cast<uint64_t *>(scratch);
   if (r > 0) {
     const int threads = chunk < kFoidThreads ? chunk : kFoidThreads;
-    if (axis == 0)
-      foid_local_kernel<0><<<static_cast<unsigned>(chunks), threads, 0, s>>>(T, rows, cols, r, chunk, cand);
+    const unsigned grid = static_cast<unsigned>(chunks);
+    if (axis == 1)
+      foid_local_kernel<1><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
+    else if (r <= 32)
+      foid_local_rows_kernel<1><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
+    else if (r <= 64)
+      foid_local_rows_kernel<2><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
+    else if (r <= 128)
+      foid_local_rows_kernel<4><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
     else
-      foid_local_kernel<1><<<static_cast<unsigned>(chunks), threads, 0, s>>>(T, rows, cols, r, chunk, cand);
+      foid_local_rows_kernel<8><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
   }
   const int runs = r > 0 ? static_cast<int>(chunks) : 0;
   if (r <= 32)
