@@ -55,6 +55,35 @@ __global__ void gather_rows_t_kernel(const uint16_t *__restrict__ T, int64_t row
     out[(q0 + q) * r + i] = tile[i][q];
   }
 }
+// mode 2 when cols % 64 == 0 and r % 32 == 0: a CTA moves 64 columns x r selected rows with
+// 16-byte loads into shared memory, then each thread writes r/4 contiguous values of one output
+// row with 16-byte stores (column reads from the tile are conflict-free: consecutive lanes read
+// consecutive columns of one row).
+__global__ void __launch_bounds__(256) gather_rows_t_vec_kernel(const uint16_t *__restrict__ T, int64_t rows,
+                                                                 int64_t cols, const int32_t *__restrict__ idx,
+                                                                 int r, uint16_t *out) {
+  __shared__ __align__(16) uint16_t tile[256][72];
+  const int64_t q0 = static_cast<int64_t>(blockIdx.x) * 64;
+  for (int t = threadIdx.x; t < r * 8; t += blockDim.x) {
+    const int i = t >> 3, c = t & 7;
+    const int64_t src = idx[i];
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (src >= 0 && src < rows) v = __ldg(reinterpret_cast<const uint4 *>(T + src * cols + q0) + c);
+    *reinterpret_cast<uint4 *>(&tile[i][8 * c]) = v;
+  }
+  __syncthreads();
+  const int q = threadIdx.x & 63, part = threadIdx.x >> 6;   // four parts of r/4 values
+  const int rp = r >> 2;
+  uint16_t *dst = out + (q0 + q) * r + part * rp;
+  for (int i = 0; i < rp; i += 8) {
+    const int ib = part * rp + i;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w[k] = static_cast<uint32_t>(tile[ib + 2 * k][q]) | (static_cast<uint32_t>(tile[ib + 2 * k + 1][q]) << 16);
+    *reinterpret_cast<uint4 *>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
 // mode 3: out[i, p] = T[p, idx[i]]   (r x rows)
 __global__ void gather_cols_t_kernel(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
                                      const int32_t *__restrict__ idx, int r, uint16_t *out) {
@@ -175,7 +204,10 @@ cudaError_t launch_gather(const uint16_t *T, int64_t rows, int64_t cols, const i
       gather_cols_kernel<<<grid_for(rows * r, 256), 256, 0, s>>>(T, rows, cols, idx, r, out);
       break;
     case 2:
-      gather_rows_t_kernel<<<static_cast<unsigned>(cols / 32), 256, 0, s>>>(T, rows, cols, idx, r, out);
+      if (cols % 64 == 0 && r % 32 == 0)
+        gather_rows_t_vec_kernel<<<static_cast<unsigned>(cols / 64), 256, 0, s>>>(T, rows, cols, idx, r, out);
+      else
+        gather_rows_t_kernel<<<static_cast<unsigned>(cols / 32), 256, 0, s>>>(T, rows, cols, idx, r, out);
       break;
     case 3:
       gather_cols_t_kernel<<<grid_for(rows * r, 256), 256, 0, s>>>(T, rows, cols, idx, r, out);

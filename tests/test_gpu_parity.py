@@ -259,3 +259,33 @@ def test_scatter_add(q, axis, dtype):
     got = dC.float().cpu().numpy()
     tol = 1e-6 if dtype == torch.float32 else 2 ** -8
     assert np.allclose(got, want, rtol=tol, atol=tol)
+
+
+# ------------------------------------------------------------------------------ outlier-slice gathers
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("shape,r", [((256, 512), 64), ((384, 1152), 32), ((320, 96), 24), ((128, 256), 8),
+                                     ((4096, 14336), 64)])
+def test_gather_bitexact(q, mode, shape, r):
+    """adahop_gather moves bf16 values without arithmetic, so every mode must match plain indexing
+    bit for bit (mode 2 covers both its vectorised path, columns % 64 == 0 and r % 32 == 0, and
+    the general one)."""
+    rows, cols = shape
+    lines = rows if mode in (0, 2) else cols
+    T = torch.randn(shape, generator=torch.Generator().manual_seed(rows + cols + r)).to(torch.bfloat16)
+    sel = torch.randperm(lines, generator=torch.Generator().manual_seed(r))[:r].sort().values
+    if r > 1:
+        sel[1] = sel[0]                                  # a repeated index is gathered twice
+    idx = sel.to(torch.int32).cuda()
+    dT = T.cuda()
+    if mode == 0:
+        want = T[sel.long(), :]
+    elif mode == 1:
+        want = T[:, sel.long()]
+    elif mode == 2:
+        want = T[sel.long(), :].t()
+    else:
+        want = T[:, sel.long()].t()
+    out = torch.full(tuple(want.shape), float("nan"), dtype=torch.bfloat16, device="cuda")
+    q.adahop_gather(dT, idx, r, mode, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu().view(torch.int16), want.contiguous().view(torch.int16))
