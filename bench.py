@@ -48,8 +48,8 @@ MX_BYTES_PER_ELEM = 0.5 + 1 / 32             # one E2M1 code + its share of an E
 # gemm_mxf4_pair_step_traffic_llama3.1-8b.md).  It describes the kernel source it was taken on
 # (sha256 over the files below); for any other source the bench reports traffic as null.
 GEMM_SOURCES = ("quantized_gemm_foid_gb300/csrc/gemm.cu", "quantized_gemm_foid_gb300/csrc/common.cuh")
-GEMM_TRAFFIC = {"source_sha256": "7f260003419d37f30a188de8f69bfd6dcd44c0f774ce4031982a724cf813ac89",
-                "bytes_per_launch": 547208936}
+GEMM_TRAFFIC = {"source_sha256": "d6a7f907543532d5641914995a5e275471250fd07257151a4c8df823bd6928bd",
+                "bytes_per_launch": 540323060}
 
 
 # ------------------------------------------------------------------------------------ helpers
@@ -450,8 +450,8 @@ class Bench:
 
 
 def host_link_gbs(device, nbytes: int = 1 << 30) -> dict:
-    """This box's pinned host <-> device copy bandwidth (best of three 1 GiB copies each way): the
-    bound the end-to-end number is read against."""
+    """This box's pinned host <-> device copy bandwidth (best of three 1 GiB copies each way, and
+    both ways at once): the bound the end-to-end number is read against."""
     g = torch.empty(nbytes, dtype=torch.uint8, device=device)
     h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     out = {}
@@ -469,7 +469,30 @@ def host_link_gbs(device, nbytes: int = 1 << 30) -> dict:
             ms = start.elapsed_time(end)
             best = ms if best is None else min(best, ms)
         out[name] = round(nbytes / best / 1e6, 1)
-    del g, h
+    # both directions at once on two streams (the e2e step copies inputs in while it copies
+    # outputs out): bytes moved in both directions over the time of the pair
+    g2 = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    best = None
+    for _ in range(3):
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        s1.wait_event(start)
+        s2.wait_event(start)
+        with torch.cuda.stream(s1):
+            g.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(g2, non_blocking=True)
+        torch.cuda.current_stream().wait_stream(s1)
+        torch.cuda.current_stream().wait_stream(s2)
+        end.record()
+        torch.cuda.synchronize()
+        ms = start.elapsed_time(end)
+        best = ms if best is None else min(best, ms)
+    out["both"] = round(2 * nbytes / best / 1e6, 1)
+    del g, h, g2, h2
     return out
 
 
@@ -881,7 +904,8 @@ def main():
         "e2e": {"value": b.flops_per_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "host_link_gbs": link,
-                "copy_bound_ms_per_step": round(max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6, 2)},
+                "copy_bound_ms_per_step": round(max(h2d / link["h2d"], d2h / link["d2h"],
+                                                    (h2d + d2h) / link["both"]) / 1e6, 2)},
         "gpu_launches": b.launches_per_step() * args.steps,
         # forward -> backward context per step: X in the wgrad orientation and W in the dgrad
         # orientation (MXFP4 codes + scales) against the bf16 copies of X a BF16 backward keeps

@@ -373,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t tile = pair; tile < num_tiles; tile += num_pairs) {
       const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
       bool ready = true;
-      if (lane == 0) ready = mbar_wait(smem_u32(&ctl.acc_full), acc_phase, abort_flag, 128);
+      // polled without back-off: this wait sits on the accumulator hand-off between tiles
+      if (lane == 0) ready = mbar_wait(smem_u32(&ctl.acc_full), acc_phase, abort_flag);
       ready = __shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0) != 0;
       if (!ready) {
         if (lane == 0) {
