@@ -48,8 +48,8 @@ MX_BYTES_PER_ELEM = 0.5 + 1 / 32             # one E2M1 code + its share of an E
 # gemm_mxf4_pair_step_traffic_llama3.1-8b.md).  It describes the kernel source it was taken on
 # (sha256 over the files below); for any other source the bench reports traffic as null.
 GEMM_SOURCES = ("quantized_gemm_foid_gb300/csrc/gemm.cu", "quantized_gemm_foid_gb300/csrc/common.cuh")
-GEMM_TRAFFIC = {"source_sha256": "d6a7f907543532d5641914995a5e275471250fd07257151a4c8df823bd6928bd",
-                "bytes_per_launch": 540323060}
+GEMM_TRAFFIC = {"source_sha256": "1148435d1707e5d421d298281514c3deaa2f96c8312ca19c683b9adbea2ef45a",
+                "bytes_per_launch": 547888140}
 
 
 # ------------------------------------------------------------------------------------ helpers
@@ -392,7 +392,9 @@ class Bench:
         each linear host->device and Y, dX, dW device->host inside the timed region.  Copies run
         on their own streams and overlap the compute of other linears: linear i's upload waits
         for the previous step's compute on its buffers, its compute waits for its upload and for
-        the previous step's download of its outputs, its download waits for its compute."""
+        the previous step's download of its outputs, its download waits for its compute.
+        Returns (ms per step, H2D bytes per step, D2H bytes per step, ms per step of the same
+        copies alone)."""
         q = self.q
         host = []
         for c in self.cases:
@@ -446,7 +448,30 @@ class Bench:
             s_down.wait_event(e)
         end.record(s_down)
         torch.cuda.synchronize()
-        return start.elapsed_time(end) / steps, h2d, d2h
+        e2e_ms = start.elapsed_time(end) / steps
+
+        # the same copies on the same buffers with no compute, both directions at once: the
+        # floor this machine's host path sets for the step (it varies between boxes)
+        def copies():
+            with torch.cuda.stream(s_up):
+                for c, h in zip(self.cases, host):
+                    for k in ("X", "W", "GY"):
+                        getattr(c, k).copy_(h[k], non_blocking=True)
+            with torch.cuda.stream(s_down):
+                for c, h in zip(self.cases, host):
+                    for k in ("Y", "dX", "dW"):
+                        h[k].copy_(getattr(c, k), non_blocking=True)
+
+        copies()
+        torch.cuda.synchronize()
+        start.record(s_up)
+        s_down.wait_event(start)
+        for _ in range(steps):
+            copies()
+        s_down.wait_stream(s_up)
+        end.record(s_down)
+        torch.cuda.synchronize()
+        return e2e_ms, h2d, d2h, start.elapsed_time(end) / steps
 
 
 def host_link_gbs(device, nbytes: int = 1 << 30) -> dict:
@@ -874,7 +899,7 @@ def main():
     if st != 0:
         raise SystemExit(f"device status {st} after the timed region")
 
-    e2e_ms, h2d, d2h = b.e2e(steps=3, warmup=1)
+    e2e_ms, h2d, d2h, copies_ms = b.e2e(steps=3, warmup=1)
     link = host_link_gbs(device)
     value = whole_job_tflops(b.flops_per_step, world, ms)
 
@@ -905,7 +930,8 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "host_link_gbs": link,
                 "copy_bound_ms_per_step": round(max(h2d / link["h2d"], d2h / link["d2h"],
-                                                    (h2d + d2h) / link["both"]) / 1e6, 2)},
+                                                    (h2d + d2h) / link["both"]) / 1e6, 2),
+                "copies_only_ms_per_step": round(copies_ms, 2)},
         "gpu_launches": b.launches_per_step() * args.steps,
         # forward -> backward context per step: X in the wgrad orientation and W in the dgrad
         # orientation (MXFP4 codes + scales) against the bf16 copies of X a BF16 backward keeps

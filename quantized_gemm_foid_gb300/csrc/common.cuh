@@ -35,6 +35,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 }
 
 // ------------------------------------------------------------------------------------------
+// Programmatic dependent launch (used by the fused MXFP4 GEMM): its CTAs may be scheduled while
+// the previous kernel on the stream is still finishing.  pdl_enter() first lets the next kernel
+// be scheduled, then waits until the previous kernel has completed and its memory operations
+// are visible; nothing before it may touch global memory.  A no-op without the launch attribute.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------------
 // mbarrier
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   cluster_sync_all();                                // barriers of both CTAs initialised
   tc_fence_after();
+  pdl_enter();                                       // the set-up above overlaps the previous kernel's tail
   const uint32_t tmem = ctl.tmem_base;
   volatile int *abort_flag = &ctl.abort_flag;
   const uint32_t peer_abort = cluster_map(smem_u32(&ctl.abort_flag), peer);
@@ -646,18 +647,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// attr must hold two entries: the cluster shape and programmatic dependent launch (pdl_enter).
 cudaLaunchConfig_t pair_launch_config(cudaLaunchAttribute *attr, unsigned grid, size_t smem, cudaStream_t s) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -668,7 +672,7 @@ int pair_capacity(int num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return num_sms / 2;
   if (cached[dev] > 0) return cached[dev];
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_launch_config(attr, static_cast<unsigned>(num_sms & ~1), gemm_smem_bytes(0), 0);
   int clusters = 0;
   if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf4_pair_kernel, &cfg) != cudaSuccess || clusters <= 0) {
@@ -687,7 +691,7 @@ cudaError_t launch_mxf4(const GemmArgs &g, const GemmMaps &maps, int num_sms, cu
   const int64_t tiles = ((g.P + PairCfg::kBM - 1) / PairCfg::kBM) * ((g.Q + BN - 1) / BN);
   const int64_t cap = pair_capacity(num_sms);
   const unsigned pairs = static_cast<unsigned>(tiles < cap ? tiles : cap);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_launch_config(attr, 2 * pairs, smem, s);
   e = cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, maps, g);
   if (e != cudaSuccess) return e;
