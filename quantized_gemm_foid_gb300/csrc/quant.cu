@@ -197,14 +197,38 @@ __device__ __forceinline__ uint64_t unpack_bf16x2(uint32_t w) {
   return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// The bf16 in half H (0 = low, 1 = high) of a pair word, widened exactly to float32.
+template <int H>
+__device__ __forceinline__ float widen_bf16(uint32_t w) {
+  return __uint_as_float(H == 0 ? (w << 16) : (w & 0xFFFF0000u));
+}
+
+// Stride-1 butterfly (a, b) -> (RN(a + b), RN(a - b)) with a the bf16 in half H of w, read by the
+// mixed-precision add / sub (a widened exactly inside the instruction, then one float32
+// rounding: the same result as widening a first), b already float32.  Returns (a + b, a - b).
+template <int H>
+__device__ __forceinline__ uint64_t bfly1_bf16(uint32_t w, float b) {
+  float s, d;
+  if (H == 0)
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, l, %3;\n\t}"
+        : "=f"(s), "=f"(d) : "r"(w), "f"(b));
+  else
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, h, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(s), "=f"(d) : "r"(w), "f"(b));
+  return pack2(s, d);
+}
+
 // Quantises one 32-block held as 16 packed registers of adjacent elements, p[j] = (x_{2j},
 // x_{2j+1}) (zeroed lines already +0) -- the order of a row of bf16 pairs, so unpacking and the
 // final E2M1 conversion need no register shuffling.  Optional orthonormal block-32 Sylvester
-// Hadamard: the stride-1 butterflies are the two lanes of each register (scalar), strides
-// 2, 4, 8, 16 pair p[j] with p[j + h/2] two lanes at a time; every lane sees the same operands in
-// the same order as the scalar definition, so the results are identical.  Then E8M0 scale from
-// the block amax and E2M1 codes; returns the scale byte and writes 16 code bytes (element i in
-// nibble i).  An all-zero block gives byte 0 and codes 0.
+// Hadamard: the caller has already applied the stride-1 butterflies (the two lanes of each
+// register, taken straight from the bf16 pairs by bfly1_bf16); strides 2, 4, 8, 16 pair p[j]
+// with p[j + h/2] two lanes at a time; every lane sees the same operands in the same order as the
+// scalar definition, so the results are identical.  Then E8M0 scale from the block amax and E2M1
+// codes; returns the scale byte and writes 16 code bytes (element i in nibble i).  An all-zero
+// block gives byte 0 and codes 0.
 //
 // Scaling: with y the transformed block, the definition computes v = RN(RN(y c) s),
 // s = 2^(127 - byte), and amax = max |RN(y c)| = RN(max |y| c) (rounding is monotonic and odd).
@@ -214,12 +238,6 @@ __device__ __forceinline__ uint64_t unpack_bf16x2(uint32_t w) {
 // zero code.  So one multiply replaces two there; elsewhere both are done.
 __device__ __forceinline__ uint32_t quantize32(uint64_t (&p)[16], int hadamard, uint4 &codes) {
   if (hadamard) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      float lo, hi;
-      unpack2(p[j], lo, hi);
-      p[j] = pack2(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
-    }
 #pragma unroll
     for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
@@ -430,13 +448,51 @@ __global__ void __launch_bounds__(kTileThreads, 6) quant_cols_kernel(QuantArgs a
 
 // ---------------------------------------------------------------------------------------------
 // dual kernel: both orientations of one tensor from a single read (prep fusion).  Tile 64 rows x
-// 128 cols staged in shared memory with 4-word row padding (conflict-free row reads and
-// column-pair reads), 128 threads, eight CTAs per SM (64 registers: the kernel is bound by
-// instruction issue, and more resident warps hide its latencies better than six did); each
-// thread quantises two 32-blocks along the tile's rows (J = cols) and one 32-row block of each
-// column of a column pair (J = rows).  Same arithmetic as the two kernels above.
+// 128 cols staged in shared memory with 4-word row padding and rows 32..63 rotated by 16 words
+// (conflict-free row reads and column-pair reads), 128 threads, eight CTAs per SM (64 registers:
+// the kernel is bound by instruction issue, and more resident warps hide its latencies better
+// than six did); each thread quantises two 32-blocks along the tile's rows (J = cols) and one
+// 32-row block of each column of a column pair (J = rows).  Lanes are paired so that every
+// 16-byte code store has its neighbour in the same 32-byte sector from the adjacent lane.  Same
+// arithmetic as the two kernels above.
 // ---------------------------------------------------------------------------------------------
 constexpr int kDualPitch = kColTile / 2 + 4;     // 32-bit words per staged row
+
+// Staged position of word w (0..63) of tile row `row`: rows 32..63 are rotated by 16 words, so
+// that the column pass, whose lane pairs read the same word of rows r and r + 32, hits 32
+// distinct banks (with the 4-word row padding alone those two rows share banks).
+__device__ __forceinline__ int dual_word(int row, int w) { return (w + ((row >> 5) << 4)) & 63; }
+
+// One 32-row block of column 2 cp + H of the staged tile (rows row0 .. row0 + 31; cp here is
+// the staged word, dual_word(row0, pair)) as packed pairs
+// of consecutive rows, rows whose bit is set in zmask zeroed (ZM); with the transform (HAD), the
+// stride-1 butterflies already applied (bfly1_bf16 on the even row's half word).
+template <int H, bool ZM, bool HAD>
+__device__ __forceinline__ void dual_col_block(const uint32_t (*tile)[kDualPitch], int row0, int cp, uint32_t zmask,
+                                               uint64_t (&p)[16]) {
+  constexpr uint32_t kHalf = H ? 0xFFFF0000u : 0x0000FFFFu;   // this column's half of each word
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    uint32_t w0 = tile[row0 + 2 * j][cp], w1 = tile[row0 + 2 * j + 1][cp];
+    if (ZM) {
+      if ((zmask >> (2 * j)) & 1u) w0 &= ~kHalf;
+      if ((zmask >> (2 * j + 1)) & 1u) w1 &= ~kHalf;
+    }
+    p[j] = HAD ? bfly1_bf16<H>(w0, widen_bf16<H>(w1)) : pack2(widen_bf16<H>(w0), widen_bf16<H>(w1));
+  }
+}
+
+template <int H>
+__device__ __forceinline__ void dual_col_load(const uint32_t (*tile)[kDualPitch], int row0, int cp, uint32_t zmask,
+                                              int hadamard, uint64_t (&p)[16]) {
+  if (hadamard) {
+    if (zmask) dual_col_block<H, true, true>(tile, row0, cp, zmask, p);
+    else dual_col_block<H, false, true>(tile, row0, cp, zmask, p);
+  } else {
+    if (zmask) dual_col_block<H, true, false>(tile, row0, cp, zmask, p);
+    else dual_col_block<H, false, false>(tile, row0, cp, zmask, p);
+  }
+}
 
 __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a, uint8_t *codes_c, uint8_t *scales_c) {
   __shared__ __align__(16) uint32_t tile[kTileRows][kDualPitch];
@@ -449,24 +505,27 @@ __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a
     const int chunk = tid + kTileThreads * k;
     const int row = chunk >> 4, cc = (chunk & 15) << 2;
     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * C + c0) + (chunk & 15));
-    *reinterpret_cast<uint4 *>(&tile[row][cc]) = v;
+    *reinterpret_cast<uint4 *>(&tile[row][dual_word(row, cc)]) = v;
   }
   __syncthreads();
-  // (1) along the rows: row tid / 2, blocks 2 (tid % 2) and 2 (tid % 2) + 1 of the tile
+  // (1) along the rows: row tid / 2, blocks (tid % 2) and (tid % 2) + 2 of the tile; the two
+  // threads of a row store adjacent 16-byte code blocks (one full 32-byte sector) and read
+  // disjoint banks
   {
     const int rr = tid >> 1;
+    const int rot = (rr >> 5) << 4;
     const int64_t row = r0 + rr;
     const bool zrow = a.zero_rows && ((a.zero_rows[row >> 5] >> (row & 31)) & 1u);
 #pragma unroll 1
     for (int b = 0; b < 2; ++b) {
-      const int bl = 2 * (tid & 1) + b;                // 32-column block inside the tile
+      const int bl = (tid & 1) + 2 * b;                // 32-column block inside the tile
       const int64_t blk = (c0 >> 5) + bl;
       uint32_t zmask = zrow ? 0xFFFFFFFFu : 0u;
       if (a.zero_cols) zmask |= a.zero_cols[blk];
       uint32_t u[16];
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(&tile[rr][16 * bl + 4 * w]);
+        const uint4 v = *reinterpret_cast<const uint4 *>(&tile[rr][(16 * bl + 4 * w + rot) & 63]);
         u[4 * w] = v.x;
         u[4 * w + 1] = v.y;
         u[4 * w + 2] = v.z;
@@ -478,18 +537,25 @@ __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a
           u[j] &= ~((((zmask >> (2 * j)) & 1u) ? 0xFFFFu : 0u) | (((zmask >> (2 * j + 1)) & 1u) ? 0xFFFF0000u : 0u));
       }
       uint64_t p[16];
+      if (a.hadamard) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) p[j] = unpack_bf16x2(u[j]);
+        for (int j = 0; j < 16; ++j) p[j] = bfly1_bf16<0>(u[j], widen_bf16<1>(u[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) p[j] = unpack_bf16x2(u[j]);
+      }
       uint4 codes;
       const uint32_t byte = quantize32(p, a.hadamard, codes);
       *reinterpret_cast<uint4 *>(a.codes + row * (C >> 1) + (blk << 4)) = codes;
       a.scales[scale_offset(a.scale_layout, row, blk, C)] = static_cast<uint8_t>(byte);
     }
   }
-  // (2) along the columns: column pair tid % 64, 32-row block tid / 64
+  // (2) along the columns: column pair tid / 2, 32-row block tid % 2; the two threads of a column
+  // store its two adjacent 16-byte code blocks (one full sector) and adjacent scale bytes
   {
-    const int cp = tid & 63;
-    const int rb = tid >> 6;
+    const int cp = tid >> 1;
+    const int rb = tid & 1;
+    const int pw = dual_word(32 * rb, cp);             // staged word of the column pair
     const int64_t blk = (r0 >> 5) + rb;
     uint32_t zr = 0;
     if (a.zero_rows) zr = a.zero_rows[(r0 + 32 * rb) >> 5];
@@ -498,25 +564,9 @@ __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a
       const int64_t line = c0 + 2 * cp + h;
       uint32_t zmask = zr;
       if (a.zero_cols && ((a.zero_cols[line >> 5] >> (line & 31)) & 1u)) zmask = 0xFFFFFFFFu;
-      const uint32_t half = h ? 0xFFFF0000u : 0x0000FFFFu;   // this column's half of each word
       uint64_t p[16];
-      if (zmask == 0u) {                                     // no zeroed rows or column: plain widening
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t w0 = tile[32 * rb + 2 * j][cp], w1 = tile[32 * rb + 2 * j + 1][cp];
-          p[j] = h ? pack2(__uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 & 0xFFFF0000u))
-                   : pack2(__uint_as_float(w0 << 16), __uint_as_float(w1 << 16));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          uint32_t w0 = tile[32 * rb + 2 * j][cp], w1 = tile[32 * rb + 2 * j + 1][cp];
-          if ((zmask >> (2 * j)) & 1u) w0 &= ~half;
-          if ((zmask >> (2 * j + 1)) & 1u) w1 &= ~half;
-          p[j] = h ? pack2(__uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 & 0xFFFF0000u))
-                   : pack2(__uint_as_float(w0 << 16), __uint_as_float(w1 << 16));
-        }
-      }
+      if (h) dual_col_load<1>(tile, 32 * rb, pw, zmask, a.hadamard, p);
+      else dual_col_load<0>(tile, 32 * rb, pw, zmask, a.hadamard, p);
       uint4 codes;
       const uint32_t byte = quantize32(p, a.hadamard, codes);
       *reinterpret_cast<uint4 *>(codes_c + line * (R >> 1) + (blk << 4)) = codes;
