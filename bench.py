@@ -595,6 +595,26 @@ def whole_job_tflops(flops_per_step_per_rank: float, world: int, ms_per_step: fl
     return flops_per_step_per_rank * world / (ms_per_step / 1e3) / 1e12
 
 
+def run_config(strategies: dict, oe_rank: int) -> dict:
+    """The `config` object of the bench line, shared by the GPU arm and the reference arm: the
+    timed workload (the Llama3.1-8B linear block, 7 linears fwd + bwd) and its calibrated plan."""
+    wl = WORKLOADS[WORKLOAD]
+    return {"workload": "llama3.1-8b linear block fwd+bwd (q,k,v,o,gate,up,down)", "M": wl.M,
+            "hidden": 4096, "kv": 1024, "ffn": 14336, "oe_rank": oe_rank, "strategies": strategies,
+            "outputs": "bf16", "l2": "no flush: every step reads and writes ~15 GB, >> 129 MB L2",
+            "flops_per_step": wl.flops_fwd_bwd()}
+
+
+def oracle_strategies(plan: dict) -> dict:
+    """The oracle plan's patterns and strategies under the names the GPU arm reports."""
+    import oracle as O
+    names = {"N": "None", "R": "Row-wise", "C": "Column-wise"}
+    pats = {k: names[O.PATTERN_LETTER[v]] for k, v in plan["patterns"].items()}
+    return {"patterns": {"X": pats["X"], "W": pats["W"], "G_Y": pats["GY"]},
+            "fwd": O.STRATEGY_NAME[plan["fwd"]], "dgrad": O.STRATEGY_NAME[plan["dgrad"]],
+            "wgrad": O.STRATEGY_NAME[plan["wgrad"]], "uniform_over_linears": True}
+
+
 def run_reference(args, world, rank):
     """Reference arm: the CPU oracle as it stands, each step one bounded sample of the workload."""
     if rank != 0:
@@ -612,9 +632,10 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic",
-            "config": {"workload": "llama3.1-8b linear block fwd+bwd (bounded CPU sample per step)"},
+            "config": run_config(oracle_strategies(cache["plan"]), cache["plan"]["oe_rank"]),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": "first 256 tokens of the k projection, Fwd + dgrad + wgrad per step"},
+                             "sample": "each step: the first 256 tokens of the k projection (N = 1024, "
+                                       "K = 4096), Fwd + dgrad + wgrad under the block's plan, rank 64"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -909,11 +930,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1 x e2m1 (MXFP4) + bf16 outliers, fp32 accumulate", "data": "synthetic",
-        "config": {"workload": "llama3.1-8b linear block fwd+bwd (q,k,v,o,gate,up,down)", "M": b.wl.M,
-                   "hidden": 4096, "kv": 1024, "ffn": 14336, "oe_rank": b.cases[0].plan.oe_rank,
-                   "strategies": b.strategies(), "outputs": "bf16",
-                   "l2": "no flush: every step reads and writes ~15 GB, >> 129 MB L2",
-                   "flops_per_step": b.flops_per_step},
+        "config": run_config(b.strategies(), b.cases[0].plan.oe_rank),
         "roofline": {"kernel": "fused MXFP4 + BF16-outlier tcgen05 GEMM", "bound": "tensor",
                      "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
                      "peak_source": f"{peak_kind}: bf16_tflops_sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
