@@ -48,7 +48,7 @@ MX_BYTES_PER_ELEM = 0.5 + 1 / 32             # one E2M1 code + its share of an E
 # gemm_mxf4_pair_step_traffic_llama3.1-8b.md).  It describes the kernel source it was taken on
 # (sha256 over the files below); for any other source the bench reports traffic as null.
 GEMM_SOURCES = ("quantized_gemm_foid_gb300/csrc/gemm.cu", "quantized_gemm_foid_gb300/csrc/common.cuh")
-GEMM_TRAFFIC = {"source_sha256": "1148435d1707e5d421d298281514c3deaa2f96c8312ca19c683b9adbea2ef45a",
+GEMM_TRAFFIC = {"source_sha256": "00c7923a024d2067f588876bf260b1d0fb89995c06b780980c103559111974ea",
                 "bytes_per_launch": 547888140}
 
 
@@ -118,11 +118,17 @@ class ClockSampler:
 
 
 def gemm_source_sha256() -> str:
+    """sha256 of the fused GEMM's sources with whole-line // comments, trailing // comments and
+    blank lines removed, so that editing a comment does not count as changing the kernel."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in GEMM_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            for line in f:
+                code = re.sub(r"\s*//.*$", "", line.rstrip("\n")).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()
 
 

@@ -30,7 +30,11 @@
 // storing, so the next tile's MMAs overlap the stores.  In the MXFP4 kernel the stores go through
 // shared memory: each epilogue warp converts 32 rows x 32 bytes of C into a 1 KB swizzled box
 // and writes it with a TMA bulk store, which turns one-row-per-lane global stores into whole
-// box writes (the J = 1024 shapes are bound by this store stream).  Every mbarrier wait is bounded
+// box writes (the J = 1024 shapes are bound by this store stream).  The MXFP4 kernel is launched
+// with programmatic dependent launch: barrier set-up and the tensor-memory allocation run while
+// the previous kernel on the stream finishes (its 212 KB of shared memory keep it off any SM that
+// still holds another GEMM's CTA), and pdl_enter() waits for that kernel before the first global
+// access.  Every mbarrier wait is bounded
 // (common.cuh); on expiry the kernel sets the status word, stops issuing work, drains what it
 // issued, frees tensor memory and returns.
 #include "common.cuh"

@@ -121,6 +121,41 @@ def test_quantize_edge_values(q):
             assert np.array_equal(to_host_u8(codes).reshape(lines, -1), wc)
 
 
+def test_quantize_dual_edge_values(q):
+    """The dual kernel on the edge values of both orientations: constant blocks (31 exact zeros
+    after the transform, where the sign of zero decides the code), negative zeros, subnormal-scale,
+    tie and huge blocks, along rows and along columns, in both 32-row halves of the staged tile."""
+    rows, cols = 128, 256
+    x = np.zeros((rows, cols), np.float32)
+    x[1, :32] = 2.0 ** -130 * np.arange(32)
+    x[2, :32] = np.array([6, 5, 3.5, 2.5, 1.75, 1.25, 0.75, 0.25] * 4, np.float32)
+    x[3, 32:64] = -x[2, :32]
+    x[4, 64:96] = 0.5                                          # constant along a row block
+    x[5, 96:128] = -0.0
+    x[6, :] = 1.0e37 * np.cos(np.arange(cols))
+    x[40, 128:160] = -3.0
+    x[33:65, 7] = 0.75                                         # constant along a column block
+    x[64:96, 9] = np.array([6, 5, 3.5, 2.5, 1.75, 1.25, 0.75, 0.25] * 4, np.float32)
+    x[96:128, 130] = 2.0 ** -135 * np.arange(32)
+    x[32:64, 200] = -0.0
+    x[:, 255] = np.float32(1.5) ** (np.arange(rows) % 64 - 32)
+    T = O.f32_to_bf16_bits(x)
+    dT = dev_bf16_from_bits(T)
+    for had in (1, 0):
+        cr = torch.zeros(rows * cols // 2, dtype=torch.uint8, device="cuda")
+        sr = torch.zeros(rows * cols // 32, dtype=torch.uint8, device="cuda")
+        cc = torch.zeros_like(cr)
+        sc = torch.zeros_like(sr)
+        q.adahop_quantize_mxfp4_dual(dT, had, None, None, cr, sr, cc, sc, 0)
+        torch.cuda.synchronize()
+        wcr, wsr = O.quantize_operand(T, bool(had))
+        wcc, wsc = O.quantize_operand(np.ascontiguousarray(T.T), bool(had))
+        assert np.array_equal(to_host_u8(cr).reshape(rows, -1), wcr)
+        assert np.array_equal(to_host_u8(sr).reshape(rows, -1), wsr)
+        assert np.array_equal(to_host_u8(cc).reshape(cols, -1), wcc)
+        assert np.array_equal(to_host_u8(sc).reshape(cols, -1), wsc)
+
+
 # ------------------------------------------------------------------------------ K1 FOID
 @pytest.mark.parametrize("axis", [0, 1])
 @pytest.mark.parametrize("shape,r", [((256, 512), 16), ((4096, 640), 64), ((128, 2560), 1),
