@@ -566,15 +566,22 @@ def cpu_baseline(budget_s: float = 12.0) -> dict:
 
 
 # ------------------------------------------------------------------------------------ main
-def dist_setup():
+def dist_setup(timeout_s: float | None = None):
+    """Joins the process group torch.distributed.run describes in the environment.  Collectives
+    are bounded by `timeout_s` (default: BENCH_PG_TIMEOUT_S, else 600 s), so a rank that died or
+    left ends the others' next barrier with an error instead of a hang."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if torch.cuda.is_available():
         torch.cuda.set_device(local)          # before NCCL binds its communicator to a device
     if world > 1:
+        from datetime import timedelta
         import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        if timeout_s is None:
+            timeout_s = float(os.environ.get("BENCH_PG_TIMEOUT_S", "600"))
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo",
+                                timeout=timedelta(seconds=timeout_s))
     return world, rank, local
 
 

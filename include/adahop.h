@@ -161,6 +161,16 @@ adahop_status adahop_linear_bwd_saved(const adahop_plan *plan, const void *GY, c
  * Returns ADAHOP_ERR_TIMEOUT if any kernel that used this workspace gave up a bounded wait. */
 adahop_status adahop_get_device_status(void *workspace, adahop_stream_t stream);
 
+/* Diagnostic of the failure path (no counterpart in the method): launches one kernel whose single
+ * thread waits, through the bounded wait every kernel of this library uses, on a shared-memory
+ * mbarrier that nothing arrives on.  The wait gives up after its limit (2 s), the kernel records
+ * the timeout in the status word of `workspace` (its first 256 bytes; ws_bytes >= 256, 256-byte
+ * aligned) and returns; no memory fault, trap or hang is involved, and the context stays usable.
+ * Asynchronous: a later adahop_get_device_status() on this workspace returns ADAHOP_ERR_TIMEOUT
+ * (and clears the word).  Host errors: ADAHOP_ERR_WORKSPACE (null or < 256 bytes),
+ * ADAHOP_ERR_ALIGN, ADAHOP_ERR_CUDA (launch failure). */
+adahop_status adahop_check_bounded_wait(void *workspace, size_t ws_bytes, adahop_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * Stage entry points (each is one step of Fig. 9; the linear calls above chain them).
  * --------------------------------------------------------------------------------------- */

@@ -50,6 +50,7 @@ PROTOTYPES = {
                                         c_void_p, c_size_t, c_int64, c_int64, c_int64, c_void_p,
                                         c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
     "adahop_get_device_status": (c_int, [c_void_p, c_void_p]),
+    "adahop_check_bounded_wait": (c_int, [c_void_p, c_size_t, c_void_p]),
     "adahop_foid": (c_int, [c_void_p, c_int64, c_int64, c_int, c_int, c_void_p, c_void_p,
                             c_void_p, c_size_t, c_void_p]),
     "adahop_foid_workspace_size": (c_size_t, [c_int64, c_int]),

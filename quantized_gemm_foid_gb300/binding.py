@@ -191,6 +191,13 @@ def adahop_get_device_status(workspace, stream=None) -> int:
     return LIB.adahop_get_device_status(_p(workspace), _stream(stream))
 
 
+def adahop_check_bounded_wait(workspace, stream=None) -> None:
+    """Launches the failure-path probe: a later adahop_get_device_status(workspace) returns
+    ADAHOP_ERR_TIMEOUT once its bounded wait (2 s) has run out."""
+    _check(LIB.adahop_check_bounded_wait(_p(workspace), workspace.numel(), _stream(stream)),
+           "adahop_check_bounded_wait")
+
+
 def adahop_foid_workspace_size(lines: int, r: int) -> int:
     return LIB.adahop_foid_workspace_size(lines, r)
 

@@ -791,6 +791,15 @@ adahop_status adahop_get_device_status(void *workspace, adahop_stream_t stream) 
   return ADAHOP_OK;
 }
 
+adahop_status adahop_check_bounded_wait(void *workspace, size_t ws_bytes, adahop_stream_t stream) {
+  if (!workspace) return ADAHOP_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return ADAHOP_ERR_ALIGN;
+  if (ws_bytes < 256) return ADAHOP_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CUDA_TRY(launch_bounded_wait_probe(static_cast<uint32_t *>(workspace), s), "bounded-wait probe launch");
+  return ADAHOP_OK;
+}
+
 size_t adahop_foid_workspace_size(int64_t lines, int r) {
   return align256(foid_scratch_bytes(lines, r));
 }

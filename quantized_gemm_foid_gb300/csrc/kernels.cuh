@@ -46,6 +46,7 @@ cudaError_t launch_gather(const uint16_t *T, int64_t rows, int64_t cols, const i
 cudaError_t launch_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype, const float *partial,
                                int splits, const int32_t *idx, int r, int axis, cudaStream_t s);
 
+cudaError_t launch_bounded_wait_probe(uint32_t *status, cudaStream_t s);
 cudaError_t launch_calib_stats(const uint16_t *T, int64_t rows, int64_t cols, float *row_ms,
                                float *col_ms, cudaStream_t s);
 

@@ -1,5 +1,5 @@
-// K4 (fused scatter-add), the outlier-slice gathers of the BF16 path, and K7 (calibration
-// statistics).
+// K4 (fused scatter-add), the outlier-slice gathers of the BF16 path, K7 (calibration
+// statistics), and the probe of the bounded-wait failure path.
 //
 // AdaHOP appendix implementation notes, "Fused Scatter-Add": the outlier product is added in
 // place into the residual GEMM's result.  Here the (possibly split-K) float32 partials are
@@ -184,6 +184,18 @@ __global__ void scale_kernel(float *v, int64_t n, float s) {
     v[t] *= s;
 }
 
+// Failure-path probe: one thread waits, through the same bounded wait the GEMM kernels use, on
+// an mbarrier that nothing ever arrives on.  The wait gives up after its limit (2 s of
+// %globaltimer); the thread records the timeout in the status word and the kernel returns, so the
+// context stays usable.
+__global__ void bounded_wait_probe_kernel(uint32_t *status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) mbar_init(smem_u32(&bar), 1);
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, nullptr)) report_status(status, kStatusTimeout);
+  __syncthreads();
+}
+
 unsigned grid_for(int64_t work, int threads, int64_t cap = 8192) {
   int64_t b = (work + threads - 1) / threads;
   if (b < 1) b = 1;
@@ -237,6 +249,11 @@ cudaError_t launch_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype, con
       scatter_cols_kernel<uint16_t><<<g, 256, 0, s>>>(static_cast<uint16_t *>(C), P, Q, partial,
                                                       splits, idx, r);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bounded_wait_probe(uint32_t *status, cudaStream_t s) {
+  bounded_wait_probe_kernel<<<1, 32, 0, s>>>(status);
   return cudaGetLastError();
 }
 

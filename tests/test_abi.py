@@ -81,6 +81,10 @@ def test_argument_errors_return_before_any_launch(lib):
                                4096, None) == 2
     assert L.adahop_scatter_add(None, 1, 1, 0, None, 1, None, 0, 0, None) == 1
     assert L.adahop_calibrate(None, None, None, 128, 128, 128, None, None, None, 0, None) == 1
+    # the failure-path probe checks its workspace on the host (7 = workspace, 3 = alignment)
+    assert L.adahop_check_bounded_wait(None, 256, None) == 7
+    assert L.adahop_check_bounded_wait(0x1010, 256, None) == 3
+    assert L.adahop_check_bounded_wait(0x1000, 128, None) == 7
 
 
 def test_python_binding_names_match_c(lib):

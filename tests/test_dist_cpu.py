@@ -50,6 +50,39 @@ def test_two_ranks_agree_on_slowest_time_and_whole_job_value():
     assert all(v == pytest.approx(2 * 1e12 / 15e-3 / 1e12) for *_, v in res)
 
 
+def _leaving_rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import time
+    import bench
+    w, r, _ = bench.dist_setup(timeout_s=10.0)
+    if r == 1:
+        os._exit(3)                                     # leaves between steps, no collective in flight
+    t0 = time.monotonic()
+    try:
+        bench.barrier(w)
+        out.put((r, "no error", time.monotonic() - t0))
+    except Exception as e:                              # the surviving rank learns of it on the host
+        out.put((r, type(e).__name__, time.monotonic() - t0))
+
+
+def test_a_rank_that_leaves_ends_the_others_barrier_with_an_error():
+    """Failure detection on the host: rank 1 exits after joining; rank 0's next barrier raises
+    within the process-group timeout instead of waiting forever."""
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    procs = [ctx.Process(target=_leaving_rank_main, args=(r, world, port, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    r, outcome, waited = out.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+    assert r == 0 and outcome != "no error"
+    assert waited < 60.0
+    assert procs[1].exitcode == 3 and procs[0].exitcode == 0
+
+
 def test_reference_arm_runs_on_rank_zero_only(capsys):
     import bench
     # a non-zero rank returns at once, prints nothing and needs no oracle work
