@@ -48,8 +48,8 @@ MX_BYTES_PER_ELEM = 0.5 + 1 / 32             # one E2M1 code + its share of an E
 # gemm_mxf4_pair_step_traffic_llama3.1-8b.md).  It describes the kernel source it was taken on
 # (sha256 over the files below); for any other source the bench reports traffic as null.
 GEMM_SOURCES = ("quantized_gemm_foid_gb300/csrc/gemm.cu", "quantized_gemm_foid_gb300/csrc/common.cuh")
-GEMM_TRAFFIC = {"source_sha256": "00c7923a024d2067f588876bf260b1d0fb89995c06b780980c103559111974ea",
-                "bytes_per_launch": 547888140}
+GEMM_TRAFFIC = {"source_sha256": "5b95a0210224c4d2da5a2a31e4348efde00a426648e8a27dc29305432bfbbadb",
+                "bytes_per_launch": 538105209}
 
 
 # ------------------------------------------------------------------------------------ helpers

@@ -90,6 +90,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
   }
 }
 
+// Teardown after a bounded wait gave up: TMA loads issued before the abort may still be landing
+// in shared memory, and in a CTA pair a CTA cannot wait for its own loads (they count on the even
+// CTA's barrier).  They land within microseconds, so one thread pauses this long (of
+// %globaltimer) while the rest of the CTA, and through the cluster barrier its peer, wait for it
+// before leaving.  Never reached on the normal path.
+constexpr uint64_t kSettleNs = 200000ull;
+
+__device__ __forceinline__ void settle_inflight_loads() {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < kSettleNs) __nanosleep(2000);
+}
+
 // ------------------------------------------------------------------------------------------
 // TMA / bulk copies (global -> shared, completion counted on an mbarrier)
 // ------------------------------------------------------------------------------------------

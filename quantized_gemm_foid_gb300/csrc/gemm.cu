@@ -451,6 +451,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   tc_fence_before();
   cluster_sync_all();
+  // After the barrier both CTAs read the same flag (a thread that gives up sets its own CTA's
+  // and its peer's before arriving), so the second barrier is taken by both or by neither.
+  if (*abort_flag) {
+    if (threadIdx.x == 0) settle_inflight_loads();
+    cluster_sync_all();
+  }
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
@@ -647,6 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {                                 // the same value for every thread after the barrier
+    if (threadIdx.x == 0) settle_inflight_loads();
+    __syncthreads();
+  }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
