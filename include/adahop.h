@@ -228,8 +228,10 @@ adahop_status adahop_quantize_mxfp4(const void *T, int64_t rows, int64_t cols, i
 /* Both orientations of adahop_quantize_mxfp4 from one read of T (prep fusion): codes_rows /
  * scales_rows receive exactly what inner_axis 1 produces (lines = rows, J = cols), codes_cols /
  * scales_cols exactly what inner_axis 0 produces (lines = cols, J = rows), with the same masks,
- * Hadamard flag and scale layout.  adahop_linear_bwd uses it for G_Y when dgrad and wgrad need
- * the same residual.  Traffic 2 + 2 x 0.53 bytes per element instead of 2 x 2.53. */
+ * Hadamard flag and scale layout.  The linear calls use it for G_Y when dgrad and wgrad need the
+ * same residual, and adahop_linear_fwd_save for X and W when the forward GEMM and the saved
+ * backward orientation share mask and Hadamard setting.  Traffic 2 + 2 x 0.53 bytes per element
+ * instead of 2 x 2.53. */
 adahop_status adahop_quantize_mxfp4_dual(const void *T, int64_t rows, int64_t cols, int hadamard,
                                          const uint32_t *zero_rows_mask,
                                          const uint32_t *zero_cols_mask, uint8_t *codes_rows,
