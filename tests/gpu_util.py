@@ -19,9 +19,11 @@ def host_bits(t: torch.Tensor) -> np.ndarray:
     return bf16_bits(t)
 
 
-def tiled_scale_permutation(lines: int, J: int) -> np.ndarray:
-    """offset[l, b] of scale (line l, block b) in the tensor-core layout (include/adahop.h)."""
-    l = np.arange(lines, dtype=np.int64)[:, None]
+def tiled_scale_permutation(lines, J: int) -> np.ndarray:
+    """offset[l, b] of scale (line l, block b) in the tensor-core layout (include/adahop.h), for
+    lines 0 .. lines - 1 (an int) or for the given line numbers (an array)."""
+    ids = np.arange(lines) if np.isscalar(lines) else np.asarray(lines)
+    l = ids.astype(np.int64)[:, None]
     b = np.arange(J // 32, dtype=np.int64)[None, :]
     return ((l >> 7) * (J >> 7) + (b >> 2)) * 512 + (l & 31) * 16 + ((l >> 5) & 3) * 4 + (b & 3)
 
@@ -33,7 +35,8 @@ def to_tiled(scales: np.ndarray) -> np.ndarray:
     return out
 
 
-def from_tiled(flat: np.ndarray, lines: int, J: int) -> np.ndarray:
+def from_tiled(flat: np.ndarray, lines, J: int) -> np.ndarray:
+    """The scales of lines 0 .. lines - 1 (an int) or of the given line numbers (an array)."""
     return np.asarray(flat)[tiled_scale_permutation(lines, J)]
 
 
