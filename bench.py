@@ -694,6 +694,28 @@ def sweep(q, device, args):
     print(json.dumps({"sweep": "llama3.1-8b down projection, Fwd", "K": K, "N": N, "points": points}))
 
 
+def outlier_splits_sweep(q, device):
+    """Split-K of the outer-OE outlier GEMM on the step's shapes, O = G_Y[idx, :] (64 x J) times W
+    (J x Q, read MN-major) into float32 partials: microseconds per launch (CUDA events, 20
+    launches) for each number of splits.  Prints one JSON object."""
+    from synthetic import normal_bf16
+    ws = q.new_workspace(4096, device=device)
+    out = {}
+    for name, P, Q, J in (("gate", 64, 4096, 14336), ("down", 64, 14336, 4096), ("q", 64, 4096, 4096),
+                          ("k", 64, 4096, 1024)):
+        A = normal_bf16(P, J, 1.0, 1, device=device)
+        B = normal_bf16(J, Q, 0.02, 2, device=device)
+        res = {}
+        for S in (1, 2, 4, 6, 8, 9, 12, 16):
+            part = torch.empty((S, P, Q), dtype=torch.float32, device=device)
+            res[S] = round(1e3 * cuda_time_ms(
+                lambda: q.adahop_gemm_bf16(A, 1, B, 0, P, Q, J, None, ws, splits=S, c_partial=part), 20), 2)
+        out[name] = res
+    if q.adahop_get_device_status(ws) != 0:
+        raise SystemExit("device status after the sweep")
+    print(json.dumps({"outlier_gemm_us_by_splits": out}), flush=True)
+
+
 def batch_sweep(q, device, args):
     """Throughput against batch size (the pages' Fig. 6 analogue): the Llama3.1-8B block's seven
     linears, Fwd + dgrad + wgrad, at M = seq_len x batch tokens per step for seq_len 4096 and
@@ -869,6 +891,8 @@ def main():
     ap.add_argument("--batch-sweep", action="store_true",
                     help="throughput against batch size (seq_len 4096, batch 1..16), AdaHOP and BF16 plans; "
                          "prints one JSON object")
+    ap.add_argument("--outlier-splits", action="store_true",
+                    help="split-K sweep of the outer-OE outlier GEMM on the step's shapes; prints one JSON object")
     ap.add_argument("--quality", action="store_true",
                     help="relative MSE of the Table 3 plans on the 8B gate projection; prints one JSON object")
     ap.add_argument("--profile", choices=["step", "gemm", "quant", "quant1", "foid", "scatter", "bf16", "outlier"],
@@ -903,6 +927,9 @@ def main():
         return
     if args.batch_sweep:
         batch_sweep(q, device, args)
+        return
+    if args.outlier_splits:
+        outlier_splits_sweep(q, device)
         return
 
     peaks, peak_kind = load_peaks()
