@@ -392,7 +392,9 @@ __device__ __forceinline__ void load_tile(const QuantArgs &a, int64_t r0, int64_
     const int chunk = tid + kTileThreads * k;
     const int row = chunk >> 4, cc = (chunk & 15) << 2;   // cc in 32-bit words
     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * a.cols + c0) + (chunk & 15));
-    *reinterpret_cast<uint4 *>(&tile[row][cc]) = v;
+    // rows 32..63 rotated by 16 words: the column pass's lane pairs read the same word of rows
+    // r and r + 32, which would otherwise share a bank
+    *reinterpret_cast<uint4 *>(&tile[row][(cc + ((row >> 5) << 4)) & 63]) = v;
   }
 }
 
@@ -401,8 +403,11 @@ __device__ __forceinline__ void quant_tile_cols(const QuantArgs &a, int64_t r0, 
                                                 uint8_t *codes, uint8_t *scales) {
   const int64_t R = a.rows;
   const int tid = threadIdx.x;
-  const int cp = tid & 63;                        // column pair
-  const int rb = tid >> 6;                        // 32-row block inside the tile
+  // lane pairs take the two 32-row blocks of one column pair, so each line's two adjacent 16-byte
+  // code blocks leave in one full 32-byte sector
+  const int cp = tid >> 1;                        // column pair
+  const int rb = tid & 1;                         // 32-row block inside the tile
+  const int pw = (cp + 16 * rb) & 63;             // its staged word (rows 32..63 rotated)
   const int64_t blk = (r0 >> 5) + rb;
   const int64_t line0 = c0 + 2 * cp;
   uint32_t zr = 0;
@@ -418,7 +423,7 @@ __device__ __forceinline__ void quant_tile_cols(const QuantArgs &a, int64_t r0, 
     float x0[32], x1[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const uint32_t w = tile[32 * rb + i][cp];
+      const uint32_t w = tile[32 * rb + i][pw];
       x0[i] = bf16_bits_to_f32(w & 0xFFFFu);
       x1[i] = bf16_bits_to_f32(w >> 16);
     }
