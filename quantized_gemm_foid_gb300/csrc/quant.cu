@@ -20,11 +20,16 @@
 // as the scalar instruction), which halves the float32 instruction count of the butterflies; at
 // HBM rate the two-orientation pass is otherwise bound by float32 issue, not by memory.
 // Work distribution (2 B read + 0.53 B written per element and orientation):
-//   rows kernel: J = columns.  One thread per 32-block: four 16-byte loads, all five butterfly
-//                stages in registers, one 16-byte code store (a warp stores 512 contiguous bytes).
-//   cols kernel: J = rows (the transposed orientation).  A 128 x 128 tile is staged in shared
+//   rows kernel: J = columns.  Each thread takes two 32-blocks of a grid-stride sequence and
+//                transforms them side by side in the two float32 lanes: 16-byte loads, all five
+//                butterfly stages in registers, 16-byte code stores (a warp's blocks are
+//                contiguous, so it stores 512 contiguous bytes).
+//   cols kernel: J = rows (the transposed orientation).  A 64 x 128 tile is staged in shared
 //                memory; each thread reads a column pair as 32-bit words and transforms one
-//                32-row block of each of the two columns in turn, in registers.
+//                32-row block of both columns side by side in the two lanes; the two threads of
+//                a column pair hold its two 32-row blocks, so their code stores fill whole
+//                32-byte sectors.
+//   dual kernel: both orientations from one staged 64 x 128 tile (described at the kernel).
 #include "common.cuh"
 #include "kernels.cuh"
 
