@@ -389,6 +389,15 @@ constexpr int kColTile = 128;                     // columns per tile
 constexpr int kTileRows = 64;                     // rows per tile (two 32-row blocks)
 constexpr int kTileThreads = 128;
 
+// 16 bytes global -> shared without passing through registers (cp.async, L1 bypassed); the
+// copies a thread issued complete at cp_async_wait_all().
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 template <int PITCH>
 __device__ __forceinline__ void load_tile(const QuantArgs &a, int64_t r0, int64_t c0, uint32_t (*tile)[PITCH]) {
   const int tid = threadIdx.x;
@@ -396,11 +405,12 @@ __device__ __forceinline__ void load_tile(const QuantArgs &a, int64_t r0, int64_
   for (int k = 0; k < 8; ++k) {                   // 1024 chunks of 16 B, 16 per tile row
     const int chunk = tid + kTileThreads * k;
     const int row = chunk >> 4, cc = (chunk & 15) << 2;   // cc in 32-bit words
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * a.cols + c0) + (chunk & 15));
     // rows 32..63 rotated by 16 words: the column pass's lane pairs read the same word of rows
     // r and r + 32, which would otherwise share a bank
-    *reinterpret_cast<uint4 *>(&tile[row][(cc + ((row >> 5) << 4)) & 63]) = v;
+    cp_async16(&tile[row][(cc + ((row >> 5) << 4)) & 63],
+               reinterpret_cast<const uint4 *>(a.T + (r0 + row) * a.cols + c0) + (chunk & 15));
   }
+  cp_async_wait_all();
 }
 
 template <int PITCH>
@@ -514,9 +524,9 @@ __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a
   for (int k = 0; k < 8; ++k) {
     const int chunk = tid + kTileThreads * k;
     const int row = chunk >> 4, cc = (chunk & 15) << 2;
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.T + (r0 + row) * C + c0) + (chunk & 15));
-    *reinterpret_cast<uint4 *>(&tile[row][dual_word(row, cc)]) = v;
+    cp_async16(&tile[row][dual_word(row, cc)], reinterpret_cast<const uint4 *>(a.T + (r0 + row) * C + c0) + (chunk & 15));
   }
+  cp_async_wait_all();
   __syncthreads();
   // (1) along the rows: row tid / 2, blocks (tid % 2) and (tid % 2) + 2 of the tile; the two
   // threads of a row store adjacent 16-byte code blocks (one full 32-byte sector) and read
