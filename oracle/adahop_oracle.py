@@ -22,25 +22,25 @@ Rotation, Kim, Khodamoradi, Denolf, Park, arXiv 2604.02525):
 * MXFP4 itself (E2M1 elements, one E8M0 scale per 32 elements) is the OCP Microscaling
   Formats v1.0 definition, which the pages name but do not restate.
 
-Readings taken where the pages are silent (each is repeated in the design notes):
+Readings taken where the pages are silent, numbered R1-R11:
 
 R1  calibration: mean-square per row and per column, ratio of the max to the lower median,
     threshold tau = 8; Column-wise if the column ratio wins, else Row-wise.
-R2  pattern pair -> strategy: CN, NN -> IHT; RC, RN -> OE-Left; NC -> OE-Right; every other
+R2, R3  pattern pair -> strategy: CN, NN -> IHT; RC, RN -> OE-Left; NC -> OE-Right; every other
     pair -> BF16.  OE-Left takes rows of the Row-wise operand (A-source if none/both),
     OE-Right takes columns of the Column-wise operand (B-source if none/both).
-R3  FOID score: population variance of the first 64 elements in float32, summed by a fixed
+R4  FOID score: population variance of the first 64 elements in float32, summed by a fixed
     pairwise tree (i + 32, then + 16, ... + 1), no fused multiply-add; ties to the lower index;
     indices returned ascending.
-R4  Hadamard: Sylvester order, orthonormal (times the float32 nearest 1/sqrt(32)), not
+R5  Hadamard: Sylvester order, orthonormal (times the float32 nearest 1/sqrt(32)), not
     randomised; butterflies with stride 1, 2, 4, 8, 16 in float32.
-R5  MX scale: E8M0 byte = clamp(floor(log2 amax) - 2 + 127, 0, 254); an all-zero block has
+R6-R8  MX scale: E8M0 byte = clamp(floor(log2 amax) - 2 + 127, 0, 254); an all-zero block has
     byte 0 and codes 0; elements round to the nearest E2M1 value, ties to the even code,
     saturating at 6; the sign bit is the element's sign bit; the even element sits in the low
     nibble.  The scale axis is the GEMM's inner dimension.
-R6  inner OE zeroes only the extracting operand; the partner keeps its lines.  The residual of
+R9, R10  inner OE zeroes only the extracting operand; the partner keeps its lines.  The residual of
     every OE strategy also gets the IHT before quantisation.
-R7  outer OE: the residual's extracted rows (columns) of C are exactly zero, so the scatter-add
+R11  outer OE: the residual's extracted rows (columns) of C are exactly zero, so the scatter-add
     result is the outlier product rounded once to the output type.
 """
 from __future__ import annotations
@@ -84,7 +84,7 @@ def f32_to_bf16_bits(x) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------------------------
-# Hadamard (reading R4)
+# Hadamard (reading R5)
 # --------------------------------------------------------------------------------------------
 def _nearest_f32_inv_sqrt32() -> np.float32:
     """The float32 value nearest 1/sqrt(32), confirmed with exact rational arithmetic.
@@ -141,7 +141,7 @@ def fwht32_f32(z) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------------------------
-# MXFP4 (reading R5; OCP MX v1.0 element and scale formats)
+# MXFP4 (readings R6-R8; OCP MX v1.0 element and scale formats)
 # --------------------------------------------------------------------------------------------
 def mx_scale_bytes(amax) -> np.ndarray:
     """E8M0 scale byte per block: clamp(floor(log2 amax) - 2 + 127, 0, 254); 0 for amax = 0.
@@ -233,7 +233,7 @@ def dequantize_operand(packed, sbytes) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------------------------
-# FOID (reading R3; Fig. 9 and the appendix FOID paragraph)
+# FOID (reading R4; Fig. 9 and the appendix FOID paragraph)
 # --------------------------------------------------------------------------------------------
 def _tree_sum_f32(v: np.ndarray) -> np.ndarray:
     """Sum along the last axis (length 64) by the fixed tree: i + 32, i + 16, ..., i + 1."""
@@ -281,7 +281,7 @@ def foid(T_bits, axis: str, r: int) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------------------------
-# Outlier Extraction split (reading R6; appendix FOID paragraph)
+# Outlier Extraction split (reading R9; appendix FOID paragraph)
 # --------------------------------------------------------------------------------------------
 def oe_split(T_bits, axis: str, idx):
     """(residual bits with the lines zeroed, outlier lines' original bits).
@@ -312,7 +312,7 @@ def oe_merge(res_bits, out_bits, axis: str, idx):
 
 
 # --------------------------------------------------------------------------------------------
-# Calibration and the strategy map (readings R1, R2; abstract, Table 1, Fig. 4, Fig. 5)
+# Calibration and the strategy map (readings R1-R3; abstract, Table 1, Fig. 4, Fig. 5)
 # --------------------------------------------------------------------------------------------
 def _ratio(s: np.ndarray) -> float:
     med = np.sort(s)[(s.size - 1) // 2]
@@ -376,7 +376,7 @@ def calibrate(X_bits, W_bits, GY_bits, tau: float = DEFAULT_TAU, oe_rank: int = 
 
 
 def oe_target(gemm: str, strategy: int, patterns: dict):
-    """(source tensor name, line axis) that OE-Left / OE-Right extracts (reading R2)."""
+    """(source tensor name, line axis) that OE-Left / OE-Right extracts (reading R3)."""
     a, b = SOURCES[gemm]
     if strategy == OE_LEFT:
         rows_wise = [s for s in (a, b) if patterns[s] == PAT_ROW]
@@ -388,7 +388,7 @@ def oe_target(gemm: str, strategy: int, patterns: dict):
 
 
 # --------------------------------------------------------------------------------------------
-# The three GEMMs (reading R6, R7; Fig. 5, Fig. 9, appendix GEMM and scatter-add paragraphs)
+# The three GEMMs (readings R9-R11; Fig. 5, Fig. 9, appendix GEMM and scatter-add paragraphs)
 # --------------------------------------------------------------------------------------------
 def gemm_operands(gemm: str, X, W, GY):
     """bf16 bit views (A: P x J, Bt: Q x J) of one GEMM; Bt is B transposed."""
