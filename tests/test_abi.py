@@ -107,3 +107,25 @@ def test_saved_size_layout(lib):
     # compression of the saved activation against its bf16 copy: 2 / (1/2 + 1/32) bytes per element
     x_part = a(K * M // 2) + a(K * M // 32)
     assert 2 * M * K / x_part == pytest.approx(2 / (0.5 + 1 / 32), rel=1e-3)
+
+
+def test_product_package_never_touches_the_oracle():
+    """The oracle is test infrastructure: nothing in the product package or its CUDA sources
+    imports, includes or names it, so no product call can route through it."""
+    pkg = os.path.join(ROOT, "quantized_gemm_foid_gb300")
+    offenders = []
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath or "__pycache__" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                if re.search(r"^\s*(import|from)\s+oracle\b|#\s*include\s*[<\"][^>\"]*oracle", text, flags=re.M):
+                    offenders.append(os.path.join(dirpath, f))
+    assert not offenders, offenders
+
+
+def test_missing_library_raises_instead_of_falling_back(lib, tmp_path):
+    from quantized_gemm_foid_gb300 import _lib
+    with pytest.raises(ImportError):
+        _lib.load_library(str(tmp_path / "libadahop.so"))
