@@ -964,7 +964,8 @@ def main():
     # with other jobs and its speed comes and goes over seconds, so three trials are timed and the
     # median one is reported, every trial listed
     e2e_trials, h2d, d2h, copy_trials = b.e2e(steps=5, warmup=5, trials=3)
-    e2e_ms = sorted(e2e_trials)[len(e2e_trials) // 2]
+    # whole job, like `value`: every rank's work over the slowest rank's (median-trial) time
+    e2e_ms = max_over_ranks(world, sorted(e2e_trials)[len(e2e_trials) // 2])
     link = host_link_gbs(device)
     value = whole_job_tflops(b.flops_per_step, world, ms)
 
@@ -987,8 +988,8 @@ def main():
                        "note": "the same step captured once in a CUDA graph and replayed"},
         "gemms": per_gemm,
         "clocks": clocks,
-        "e2e": {"value": b.flops_per_step / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+        "e2e": {"value": whole_job_tflops(b.flops_per_step, world, e2e_ms), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world, "ms_per_step": e2e_ms,
                 "host_link_gbs": link,
                 "copy_bound_ms_per_step": round(max(h2d / link["h2d"], d2h / link["d2h"],
                                                     (h2d + d2h) / link["both"]) / 1e6, 2),
