@@ -996,7 +996,7 @@ def main():
                 "trials_ms_per_step": [round(x, 2) for x in e2e_trials],
                 "copies_only_ms_per_step": [round(x, 2) for x in copy_trials],
                 "value_from": "the median of the trials"},
-        "gpu_launches": b.launches_per_step() * args.steps,
+        "gpu_launches": b.launches_per_step() * args.steps * world,   # all ranks' timed launches
         # forward -> backward context per step: X in the wgrad orientation and W in the dgrad
         # orientation (MXFP4 codes + scales) against the bf16 copies of X a BF16 backward keeps
         "saved_context": {"bytes_per_step": sum(c.saved_bytes(q) for c in b.cases),
