@@ -48,3 +48,22 @@ def test_reference_arm_reports_the_gpu_arms_config():
                             "uniform_over_linears": True}, 64)
     assert ref == gpu
     assert gpu["flops_per_step"] == 42880953483264            # 6 M N K over the seven linears
+
+
+def test_reference_arm_line_carries_the_contract_keys(capsys):
+    """One oracle step of the reference arm on rank 0: the line has every key the driver reads,
+    the GPU arm's metric, unit and config, and a zero-copy e2e of its own value."""
+    import json
+    import types
+    args = types.SimpleNamespace(steps=1, warmup=0, gpus=1)
+    bench.run_reference(args, 1, 0)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "TFLOP/s"
+    assert line["higher_is_better"] is True and line["value"] > 0
+    assert line["config"]["workload"].startswith("llama3.1-8b linear block")
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
