@@ -268,3 +268,30 @@ def adahop_calibration_stats(T, row_ms, col_ms, stream=None) -> None:
     rows, cols = T.shape
     _check(LIB.adahop_calibration_stats(_p(T), rows, cols, _p(row_ms), _p(col_ms), _stream(stream)),
            "adahop_calibration_stats")
+
+
+# ------------------------------------------------------------------------------- peak probes (K8)
+MMA_KIND_NAMES = {0: "kind::f16", 1: "kind::mxf4 (2X)", 2: "kind::mxf4nvf4 (2X)", 3: "kind::mxf4nvf4 (4X)"}
+MMA_K_PER_INSTR = {0: 16, 1: 64, 2: 64, 3: 64}
+
+
+def adahop_probe_ctas() -> int:
+    return int(LIB.adahop_probe_ctas())
+
+
+def adahop_probe_mma_rate(kind: int, sf_copies: int, iters: int, out, ws, stream=None) -> None:
+    """Launches the tensor-pipe rate probe; `out` is a uint64 (int64) device tensor of at least
+    3 * adahop_probe_ctas() entries (per CTA: loop cycles, start ns, end ns)."""
+    _cuda(out, "out")
+    _check(LIB.adahop_probe_mma_rate(int(kind), int(sf_copies), int(iters), _p(out),
+                                     out.numel() * out.element_size(), _p(ws), ws.numel(), _stream(stream)),
+           "adahop_probe_mma_rate")
+
+
+def adahop_probe_copy(src, dst, stream=None) -> None:
+    _cuda(src, "src")
+    _cuda(dst, "dst")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() < nbytes:
+        raise ValueError("dst is smaller than src")
+    _check(LIB.adahop_probe_copy(_p(src), _p(dst), nbytes, _stream(stream)), "adahop_probe_copy")

@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libadahop.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
-SOURCES = ["adahop.cu", "quant.cu", "foid.cu", "misc.cu", "gemm.cu"]
+SOURCES = ["adahop.cu", "quant.cu", "foid.cu", "misc.cu", "gemm.cu", "probe.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                 "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

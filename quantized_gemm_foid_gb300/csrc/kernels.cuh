@@ -50,6 +50,12 @@ cudaError_t launch_bounded_wait_probe(uint32_t *status, cudaStream_t s);
 cudaError_t launch_calib_stats(const uint16_t *T, int64_t rows, int64_t cols, float *row_ms,
                                float *col_ms, cudaStream_t s);
 
+// K8 peak probes.  kind: 0 kind::f16, 1 kind::mxf4 (2X), 2 kind::mxf4nvf4 (2X), 3 kind::mxf4nvf4
+// (4X); `ctas` CTAs (one per SM) each write {loop cycles, start ns, end ns} to out[3 * cta ..].
+cudaError_t launch_mma_rate_probe(int kind, int sf_copies, int64_t iters, uint64_t *out, uint32_t *status,
+                                  int ctas, cudaStream_t s);
+cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, int num_sms, cudaStream_t s);
+
 // tcgen05 GEMM (K3 MXFP4 + inner BF16 tail, K5/K6 BF16).
 struct GemmArgs {
   int64_t P, Q, J;            // C is P x Q; inner dimension J
