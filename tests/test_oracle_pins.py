@@ -391,3 +391,48 @@ def test_fig3_iht_helps_only_when_aligned():
     assert min(inner) > 15.0 and np.mean(inner) > 20.0, inner
     assert abs(np.mean(outer)) < 5.0, outer
     assert min(inner) > max(outer), (inner, outer)
+
+
+# ---------------------------------------------------------------------------------- error metrics
+def _metric_cases(golden_dir):
+    cases, cur = [], None
+    with open(os.path.join(golden_dir, "error_metrics_worked.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            if key == "case":
+                cur = {"name": rest}
+                cases.append(cur)
+            elif key in ("R", "C"):
+                cur[key] = np.array([[float(v) for v in row.split()] for row in rest.split("|")])
+            else:
+                cur[key] = float(rest)
+    return cases
+
+
+def test_error_metrics_hand_worked(golden_dir):
+    """rel_mse and rel_frobenius against values worked by hand (tests/golden/): a dropped square
+    root, a missing square, normalising by C instead of the reference, or a sign slip in C - R
+    each changes at least one case by far more than the tolerance."""
+    cases = _metric_cases(golden_dir)
+    assert len(cases) == 5
+    for c in cases:
+        assert O.rel_mse(c["C"], c["R"]) == pytest.approx(c["rel_mse"], rel=1e-12, abs=1e-300), c["name"]
+        assert O.rel_frobenius(c["C"], c["R"]) == pytest.approx(c["rel_frobenius"], rel=1e-12, abs=1e-300), c["name"]
+
+
+def test_error_metrics_invariants():
+    """Scale invariance (both metrics are ratios), the square-root relation, and independence of
+    the layout of the elements (a reshape or a transpose changes nothing)."""
+    rng = np.random.default_rng(0)
+    R = rng.standard_normal((7, 5))
+    C = R + 1e-3 * rng.standard_normal((7, 5))
+    m, f = O.rel_mse(C, R), O.rel_frobenius(C, R)
+    assert f == pytest.approx(np.sqrt(m), rel=1e-14)
+    for s in (1e-6, 3.0, 1e6):
+        assert O.rel_mse(s * C, s * R) == pytest.approx(m, rel=1e-12)
+        assert O.rel_frobenius(s * C, s * R) == pytest.approx(f, rel=1e-12)
+    assert O.rel_frobenius(C.T, R.T) == pytest.approx(f, rel=1e-14)
+    assert O.rel_frobenius(C.reshape(5, 7), R.reshape(5, 7)) == pytest.approx(f, rel=1e-14)
