@@ -40,13 +40,14 @@ METRIC = "AdaHOP linear fwd+bwd eff. TFLOPS vs MXFP4 peak; prep-kernel HBM GB/s"
 WORKLOAD = "llama3.1-8b"
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor throughput on GB300
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# vendor figures, context only (dense FP4 tensor TFLOP/s, HBM3e GB/s)
+NOMINAL = {"fp4_tflops": 13500.0, "hbm_gbs": 7900.0}
 QUANT_BYTES_PER_ELEM = 2 + 0.5 + 1 / 32   # bf16 read + E2M1 write + E8M0 write
 MX_BYTES_PER_ELEM = 0.5 + 1 / 32             # one E2M1 code + its share of an E8M0 scale
 
-# DRAM traffic of the fused GEMM per launch, averaged over the 21 launches of one step, from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/
-# gemm_mxf4_pair_step_traffic_llama3.1-8b.md).  It describes the kernel source it was taken on
-# (sha256 over the files below); for any other source the bench reports traffic as null.
+# DRAM traffic of the fused GEMM per launch, averaged over the 21 launches of one step, from ncu
+# captures (dram__bytes_read.sum + dram__bytes_write.sum).  It describes the kernel source it was
+# taken on (sha256 over the files below); for any other source the bench reports traffic as null.
 GEMM_SOURCES = ("quantized_gemm_foid_gb300/csrc/gemm.cu", "quantized_gemm_foid_gb300/csrc/common.cuh")
 GEMM_TRAFFIC = {"source_sha256": "5b95a0210224c4d2da5a2a31e4348efde00a426648e8a27dc29305432bfbbadb",
                 "bytes_per_launch": 538105209}
@@ -526,6 +527,70 @@ def host_link_gbs(device, nbytes: int = 1 << 30) -> dict:
     return out
 
 
+# ------------------------------------------------------------------------------------ peak probes (K8)
+def pipe_probe(q, kind: int = 1, sf_copies: int = 1, reps: int = 3, iters: int = 20000) -> dict:
+    """The tensor pipe's own rate for one MMA kind (K8: back-to-back tcgen05.mma on resident
+    shared-memory operands, one CTA per SM).  Default: kind::mxf4 with the six scale-factor copies
+    the fused GEMM issues per 256-wide J slice.  Median of `reps` launches: FLOP per clock per SM
+    (from clock64), the SM clock it ran at (cycles / %globaltimer) and TFLOP/s over the launch."""
+    ctas = q.adahop_probe_ctas()
+    out = torch.zeros(3 * ctas, dtype=torch.int64, device="cuda")
+    ws = q.new_workspace(256)
+    flop = 4 * 2 * 128 * 256 * q.MMA_K_PER_INSTR[kind] * iters
+    per_clk, mhz, tflops = [], [], []
+    for _ in range(reps):
+        q.adahop_probe_mma_rate(kind, sf_copies, iters, out, ws)
+        torch.cuda.synchronize()
+        if q.adahop_get_device_status(ws) != 0:
+            raise SystemExit("mma rate probe: a bounded wait ran out")
+        rec = out.view(ctas, 3).cpu().double()
+        per_clk.append(float((flop / rec[:, 0]).median()))
+        mhz.append(float((rec[:, 0] / (rec[:, 2] - rec[:, 1])).median()) * 1e3)
+        tflops.append(flop * ctas / (float(rec[:, 2].max() - rec[:, 1].min()) / 1e9) / 1e12)
+    return {"kind": q.MMA_KIND_NAMES[kind] + (" + per-slice scale copies" if sf_copies and kind else ""),
+            "flop_per_clk_per_sm": round(statistics.median(per_clk), 1), "sms": ctas,
+            "sm_mhz": round(statistics.median(mhz), 1), "tflops": round(statistics.median(tflops), 1)}
+
+
+def copy_probe(q, device, nbytes: int = 2 << 30, reps: int = 5) -> float:
+    """HBM read + write GB/s of the library's streaming copy (K8), best of `reps` 2 GiB copies."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    q.adahop_probe_copy(src, dst)
+    best = min(cuda_time_ms(lambda: q.adahop_probe_copy(src, dst), 1) for _ in range(reps))
+    del src, dst
+    return round(2 * nbytes / best / 1e6, 1)
+
+
+def roofline_fields(achieved: float, peaks: dict, peak_kind: str, pipe: dict, gemm_mhz) -> dict:
+    """The fused GEMM's roofline.  It is timed alone (one launch after another), so `peak` is the
+    burst BF16 figure times the nominal dense FP4:BF16 ratio; beside it, the K8 probe's own
+    kind::mxf4 rate on this GPU, the same rate at the SM clock sampled while the GEMMs ran
+    (time x clock: the clock-normalised fraction), and the nominal vendor figure."""
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * FP4_OVER_BF16
+    per_clk_peak = pipe["flop_per_clk_per_sm"] * pipe["sms"]
+    clk = {"sm_mhz_during_gemm": gemm_mhz, "flop_per_clk_per_sm": None, "frac": None}
+    if gemm_mhz:
+        clk["flop_per_clk_per_sm"] = round(achieved * 1e12 / (gemm_mhz * 1e6) / pipe["sms"], 1)
+        clk["frac"] = round(achieved * 1e12 / (gemm_mhz * 1e6) / per_clk_peak, 4)
+    return {"kernel": "fused MXFP4 + BF16-outlier tcgen05 GEMM", "bound": "tensor",
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": f"{peak_kind}: bf16_tflops (burst; the GEMM is timed alone) x "
+                           f"{FP4_OVER_BF16:g} (nominal dense FP4:BF16 ratio)",
+            "pipe_probe": dict(pipe, frac=round(achieved / pipe["tflops"], 4),
+                               note="K8: the tensor pipe's own kind::mxf4 rate on this GPU"),
+            "clock_normalised": clk,
+            "nominal": {"peak": NOMINAL["fp4_tflops"], "frac": round(achieved / NOMINAL["fp4_tflops"], 4)}}
+
+
+def peaks_report(q, device) -> dict:
+    """Every MMA kind the probe knows (with and without the per-slice scale copies) and the copy."""
+    rates = {}
+    for kind, sf in ((0, 0), (1, 0), (1, 1), (2, 0), (2, 1), (3, 0)):
+        rates[f"{q.MMA_KIND_NAMES[kind]}{' +sf' if sf else ''}"] = pipe_probe(q, kind, sf)
+    return {"mma": rates, "copy_gbs": copy_probe(q, device)}
+
+
 # ------------------------------------------------------------------------------------ CPU oracle
 def oracle_sample_step(cache: dict) -> tuple[float, int]:
     """One bounded sample of the workload through the CPU oracle: the first 256 tokens of the
@@ -550,18 +615,136 @@ def oracle_sample_step(cache: dict) -> tuple[float, int]:
     return dt, 6 * M * N * K
 
 
-def cpu_baseline(budget_s: float = 12.0) -> dict:
-    cache, times, flops = {}, [], 0
-    oracle_sample_step(cache)                      # warm caches, draw the sample
-    t_end = time.perf_counter() + budget_s
-    while time.perf_counter() < t_end or not times:
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or the machine type."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def _quantise_rows(args):
+    """One process-pool task: the oracle's quantiser on a block of whole rows (exact: every
+    32-element block lies inside one row)."""
+    import oracle as O
+    block, hadamard = args
+    return O.quantize_operand(block, hadamard)
+
+
+def cpu_worker(threads: int) -> dict:
+    """Times the oracle as it stands, in a process whose BLAS thread count the parent fixed
+    (`threads`, 1 or all cores), on bounded samples of the Llama3.1-8B step:
+    * sample: the oracle's whole path (quantisation, FOID, the float64 products) for Fwd + dgrad +
+      wgrad of the first 256 tokens of the k projection (the reference arm's step);
+    * prep, in full on stated tensors: IHT + MXFP4 quantisation of the q projection's W
+      (4096 x 4096; with all cores, blocks of rows on a process pool) and FOID over the 32768-row
+      probe of a Row-wise G_Y;
+    * product step: the float64 products deq(A) . deq(B) on 256-row output slices of the k
+      projection's three GEMMs (the wgrad slice has the full J = 32768)."""
+    import oracle as O
+    from synthetic import bf16_bits, normal_bf16
+    res = {"threads": threads}
+    cache = {}
+    oracle_sample_step(cache)
+    times, flops = [], 0
+    t_end = time.perf_counter() + 4.0
+    while time.perf_counter() < t_end or len(times) < 2:
         dt, flops = oracle_sample_step(cache)
         times.append(dt)
-    mean = sum(times) / len(times)
-    return {"value": flops / mean / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "first 256 tokens of the Llama3.1-8B k projection (N=1024, K=4096): Fwd IHT + dgrad "
-                      "OE-Left outer + wgrad OE-Left inner, rank 64, quantisation included; NumPy "
-                      f"(BLAS threads for the float64 products); mean of {len(times)} runs"}
+    res["sample"] = {"flops": flops, "s": statistics.median(times), "runs": len(times)}
+
+    W = bf16_bits(normal_bf16(4096, 4096, 0.02, 1))
+    t0 = time.perf_counter()
+    if threads == 1:
+        O.quantize_operand(W, True)
+    else:
+        import multiprocessing as mp
+        chunks = [(W[i:i + 256], True) for i in range(0, W.shape[0], 256)]
+        with mp.get_context("spawn").Pool(threads) as pool:
+            pool.map(_quantise_rows, chunks[:threads])          # start-up outside the timing
+            t0 = time.perf_counter()
+            pool.map(_quantise_rows, chunks)
+    res["quant"] = {"elements": int(W.size), "s": time.perf_counter() - t0, "tensor": "W of q, 4096 x 4096"}
+
+    G = bf16_bits(normal_bf16(32768, 64, 1e-3, 3, outlier_axis="row", outlier_count=64, outlier_scale=40.0))
+    t0 = time.perf_counter()
+    O.foid(G, "row", 64)
+    res["foid"] = {"lines": 32768, "r": 64, "s": time.perf_counter() - t0}
+
+    rng = np.random.default_rng(0)
+    gflop, gsec = 0, 0.0
+    for P, Q, J in ((256, 1024, 4096), (256, 4096, 1024), (256, 4096, 32768)):
+        A = rng.standard_normal((P, J))
+        B = rng.standard_normal((J, Q))
+        t0 = time.perf_counter()
+        _ = A @ B
+        gsec += time.perf_counter() - t0
+        gflop += 2 * P * Q * J
+    res["gemm"] = {"flops": gflop, "s": gsec}
+    return res
+
+
+def cpu_baseline() -> dict:
+    """The oracle timed on this host's cores, single-threaded and on all cores (two child
+    processes, BLAS threads fixed by the environment before NumPy loads), ~20-40 s of CPU work.
+    `value` is the all-core sample (the oracle's whole path on 256 tokens of the k projection,
+    Fwd + dgrad + wgrad); the prep and product figures beside it extrapolate a whole step."""
+    cores = os.cpu_count() or 1
+    runs = {}
+    for threads in (1, cores):
+        env = dict(os.environ)
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[k] = str(threads)
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", str(threads)],
+                             capture_output=True, text=True, env=env, timeout=600)
+        if out.returncode != 0:
+            raise SystemExit(f"cpu baseline worker failed:\n{out.stderr[-2000:]}")
+        runs[threads] = json.loads(out.stdout.strip().splitlines()[-1])
+    wl = WORKLOADS[WORKLOAD]
+    flops_step = wl.flops_fwd_bwd()
+    # quantisation work of one step as the oracle does it: every GEMM quantises both operands
+    quant_elems = sum(2 * (wl.M * l.K + l.N * l.K + wl.M * l.N) for l in wl.linears)
+
+    def summary(r):
+        s, qn, g = r["sample"], r["quant"], r["gemm"]
+        q_rate = qn["elements"] / qn["s"]
+        g_rate = g["flops"] / g["s"]
+        step_s = quant_elems / q_rate + flops_step / g_rate
+        return {"threads": r["threads"], "sample_tflops": s["flops"] / s["s"] / 1e12,
+                "sample_s": round(s["s"], 3), "sample_runs": s["runs"],
+                "quant_melem_per_s": round(q_rate / 1e6, 2),
+                "quant_gbs": round(q_rate * QUANT_BYTES_PER_ELEM / 1e9, 4),
+                "foid_ms": round(r["foid"]["s"] * 1e3, 2),
+                "fp64_product_gflops": round(g_rate / 1e9, 1),
+                "extrapolated_step_s": round(step_s, 1),
+                "extrapolated_tflops": flops_step / step_s / 1e12}
+    one, allc = summary(runs[1]), summary(runs[cores])
+    return {"value": allc["sample_tflops"], "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(), "nproc": cores,
+            "sample": "the oracle's whole path (IHT + MXFP4 quantisation, FOID, OE, float64 products) on the "
+                      "first 256 tokens of the Llama3.1-8B k projection (N=1024, K=4096): Fwd IHT + dgrad "
+                      "OE-Left outer + wgrad OE-Left inner, rank 64; value = all cores (BLAS threads), median "
+                      f"of {runs[cores]['sample']['runs']} runs",
+            "single_thread": one, "all_cores": allc,
+            "prep_full": {"quantise": "IHT + MXFP4 of the q projection's W (4096 x 4096) in full; all cores = "
+                                      "blocks of 256 rows on a process pool",
+                          "foid": "FOID over the 32768-row probe of a Row-wise G_Y in full (r = 64)"},
+            "extrapolated": "label: extrapolated.  Whole-step time = the step's quantisation work "
+                            f"({quant_elems / 1e9:.2f} G elements, both operands of all 21 GEMMs) at the measured "
+                            "quantisation rate + its 42.9 TFLOP at the measured float64 product rate (256-row "
+                            "output slices of the k projection's Fwd, dgrad and wgrad products)"}
 
 
 # ------------------------------------------------------------------------------------ main
@@ -646,8 +829,11 @@ def run_reference(args, world, rank):
             "data": "synthetic",
             "config": run_config(oracle_strategies(cache["plan"]), cache["plan"]["oe_rank"]),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": "each step: the first 256 tokens of the k projection (N = 1024, "
-                                       "K = 4096), Fwd + dgrad + wgrad under the block's plan, rank 64"},
+                             "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+                             "threads": "BLAS default (all cores) for the float64 products",
+                             "sample": "each step: the oracle's whole path on the first 256 tokens of the k "
+                                       "projection (N = 1024, K = 4096), Fwd + dgrad + wgrad under the block's "
+                                       "plan, rank 64"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -905,7 +1091,13 @@ def main():
                          "(r = 64); 'scatter' = three scatter-adds of 64 rows into 32768 x 4096; 'bf16' = "
                          "three BF16 GEMMs 32768 x 4096 x 4096; 'outlier' = three split-K BF16 GEMMs "
                          "64 x 4096 x 14336 (8 splits)")
+    ap.add_argument("--peaks", action="store_true",
+                    help="K8 probes only: every MMA kind's rate and the streaming copy; prints one JSON object")
+    ap.add_argument("--cpu-worker", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_worker is not None:             # child of cpu_baseline(): CPU only, no CUDA
+        print(json.dumps(cpu_worker(args.cpu_worker)), flush=True)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
@@ -918,6 +1110,9 @@ def main():
     import quantized_gemm_foid_gb300 as q
     if args.profile:
         profile(q, device, args)
+        return
+    if args.peaks:
+        print(json.dumps(peaks_report(q, device)), flush=True)
         return
     if args.sweep:
         sweep(q, device, args)
@@ -950,7 +1145,12 @@ def main():
     ms = cuda_time_ms(b.step, args.steps)
     barrier(world)
     ms = max_over_ranks(world, ms)
+    gemm_clocks = ClockSampler(gpu_index)
+    gemm_clocks.start()
     gflops, gsec, per_gemm, gbytes = b.gemm_roofline()
+    gclk = gemm_clocks.stop()
+    pipe = pipe_probe(q)
+    copy_gbs = copy_probe(q, device)
     prep = b.prep_bandwidth()
     variants = b.variants()
     g_ms = b.graph_ms()
@@ -969,20 +1169,20 @@ def main():
     link = host_link_gbs(device)
     value = whole_job_tflops(b.flops_per_step, world, ms)
 
-    fp4_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * FP4_OVER_BF16
     achieved = gflops / gsec / 1e12
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1 x e2m1 (MXFP4) + bf16 outliers, fp32 accumulate", "data": "synthetic",
         "config": run_config(b.strategies(), b.cases[0].plan.oe_rank),
-        "roofline": {"kernel": "fused MXFP4 + BF16-outlier tcgen05 GEMM", "bound": "tensor",
-                     "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
-                     "peak_source": f"{peak_kind}: bf16_tflops_sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
-                     "traffic": gemm_traffic(), "traffic_unit": "bytes per launch (DRAM, ncu)",
-                     "algorithmic_bytes": gbytes / max(1, len(per_gemm)), "launches": len(per_gemm)},
-        "prep": {"kernel": "IHT + MXFP4 quantiser", "bound": "hbm", "peak_gbs": peaks.get("hbm_gbs"),
-                 **{k: dict(v, frac=round(v["gbs"] / peaks.get("hbm_gbs", 6800.0), 3)) for k, v in prep.items()}},
+        "roofline": dict(roofline_fields(achieved, peaks, peak_kind, pipe, gclk.get("sm_mhz")),
+                         traffic=gemm_traffic(), traffic_unit="bytes per launch (DRAM, ncu)",
+                         algorithmic_bytes=gbytes / max(1, len(per_gemm)), launches=len(per_gemm)),
+        "prep": {"kernel": "IHT + MXFP4 quantiser", "bound": "hbm", "peak_gbs": hbm, "peak_source": peak_kind,
+                 "copy_probe_gbs": copy_gbs, "nominal_gbs": NOMINAL["hbm_gbs"],
+                 **{k: dict(v, frac=round(v["gbs"] / hbm, 3), frac_copy_probe=round(v["gbs"] / copy_gbs, 3),
+                            frac_nominal=round(v["gbs"] / NOMINAL["hbm_gbs"], 3)) for k, v in prep.items()}},
         "variants": variants,
         "cuda_graph": {"ms_per_step": g_ms, "value": b.flops_per_step / (g_ms / 1e3) / 1e12,
                        "note": "the same step captured once in a CUDA graph and replayed"},

@@ -67,3 +67,21 @@ def test_reference_arm_line_carries_the_contract_keys(capsys):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_roofline_peak_is_the_burst_bf16_figure_times_the_nominal_ratio():
+    """The fused GEMM is timed alone, so its peak is MEASURED_PEAKS' burst BF16 figure x 6 (not the
+    sustained one), and every fraction recomputes from the line's own fields."""
+    peaks = {"bf16_tflops": 1920.8, "bf16_tflops_sustained": 1730.4, "hbm_gbs": 6793.1}
+    pipe = {"flop_per_clk_per_sm": 32768.0, "sms": 152, "sm_mhz": 1957.0, "tflops": 9746.0}
+    r = bench.roofline_fields(7265.0, peaks, "measured", pipe, 1850.0)
+    assert r["peak"] == 1920.8 * 6
+    assert abs(r["frac"] - 7265.0 / (1920.8 * 6)) < 1e-12
+    assert abs(r["pipe_probe"]["frac"] - round(7265.0 / 9746.0, 4)) < 1e-12
+    assert abs(r["clock_normalised"]["frac"] - round(7265e12 / 1850e6 / (32768 * 152), 4)) < 1e-12
+    assert r["nominal"]["peak"] == 13500.0
+    assert bench.roofline_fields(7265.0, peaks, "measured", pipe, None)["clock_normalised"]["frac"] is None
+
+
+def test_cpu_model_is_named():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
