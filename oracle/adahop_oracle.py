@@ -390,14 +390,20 @@ def oe_target(gemm: str, strategy: int, patterns: dict):
 # --------------------------------------------------------------------------------------------
 # The three GEMMs (readings R9-R11; Fig. 5, Fig. 9, appendix GEMM and scatter-add paragraphs)
 # --------------------------------------------------------------------------------------------
-def gemm_operands(gemm: str, X, W, GY):
-    """bf16 bit views (A: P x J, Bt: Q x J) of one GEMM; Bt is B transposed."""
+def gemm_operands(gemm: str, X, W, GY, rows=None, cols=None):
+    """bf16 bit views (A: P x J, Bt: Q x J) of one GEMM; Bt is B transposed.  ``rows`` / ``cols``
+    (index arrays, or None for all) select lines of A / Bt without forming the others."""
+    def take(T, lines, transpose):
+        T = np.asarray(T)
+        if transpose:
+            return np.ascontiguousarray((T if lines is None else T[:, lines]).T)
+        return T if lines is None else T[lines]
     if gemm == "fwd":
-        return X, W
+        return take(X, rows, False), take(W, cols, False)
     if gemm == "dgrad":
-        return GY, np.ascontiguousarray(np.asarray(W).T)
+        return take(GY, rows, False), take(W, cols, True)
     if gemm == "wgrad":
-        return np.ascontiguousarray(np.asarray(GY).T), np.ascontiguousarray(np.asarray(X).T)
+        return take(GY, rows, True), take(X, cols, True)
     raise ValueError(gemm)
 
 
@@ -415,25 +421,33 @@ def gemm_plan(gemm: str, strategy: int, patterns: dict, r: int, tensors: dict):
 
 
 def gemm_oracle(gemm: str, strategy: int, X, W, GY, *, patterns=None, r: int = DEFAULT_RANK,
-                rows=None, oe=None):
+                rows=None, cols=None, oe=None):
     """Everything one AdaHOP GEMM computes, in plain NumPy (float64 for the products).
 
-    ``X`` (M x K), ``W`` (N x K), ``GY`` (M x N) are bf16 bit arrays.  ``rows`` restricts the
-    output to a subset of C's rows (the quantised B operand is still computed in full).
-    ``oe`` may pass a pre-resolved OE plan (as returned by ``gemm_plan``).
+    ``X`` (M x K), ``W`` (N x K), ``GY`` (M x N) are bf16 bit arrays.  ``rows`` / ``cols``
+    restrict the output to a subset of C's rows / columns: every line is quantised on its own
+    (its blocks run along J), so only the A lines of the requested rows and the B lines of the
+    requested columns are formed and quantised.  ``oe`` may pass a pre-resolved OE plan (as
+    returned by ``gemm_plan``; FOID always ranks every line of its source).
 
-    Returns a dict: ``C`` (float64, len(rows) x Q), ``qa``/``qb`` (packed codes, scales) of the
-    quantised operands (``qa`` only for the requested rows), ``oe`` (the resolved OE plan or
-    None), ``a_o``/``b_o`` (inner OE slices, bf16 bits) and ``o`` (outer OE product, float64).
+    Returns a dict: ``C`` (float64, len(rows) x len(cols)), ``qa``/``qb`` (packed codes, scales)
+    of the quantised operand lines, ``oe`` (the resolved OE plan or None), ``a_o``/``b_o`` (inner
+    OE slices of those lines, bf16 bits) and ``o`` (outer OE product, float64).
     """
     tensors = {"X": X, "W": W, "GY": GY}
-    A, Bt = gemm_operands(gemm, X, W, GY)
-    P, J = A.shape
+    A, Bt = gemm_operands(gemm, X, W, GY, rows, cols)
+    if gemm == "fwd":
+        P, Q = np.asarray(X).shape[0], np.asarray(W).shape[0]
+    elif gemm == "dgrad":
+        P, Q = np.asarray(GY).shape[0], np.asarray(W).shape[1]
+    else:
+        P, Q = np.asarray(GY).shape[1], np.asarray(X).shape[1]
     rows = np.arange(P) if rows is None else np.asarray(rows, dtype=np.int64)
+    cols = np.arange(Q) if cols is None else np.asarray(cols, dtype=np.int64)
     out = {"oe": None, "qa": None, "qb": None, "a_o": None, "b_o": None, "o": None}
 
     if strategy == BF16:
-        out["C"] = bf16_to_f32(A[rows]).astype(np.float64) @ bf16_to_f32(Bt).astype(np.float64).T
+        out["C"] = bf16_to_f32(A).astype(np.float64) @ bf16_to_f32(Bt).astype(np.float64).T
         return out
 
     hadamard = strategy != MXFP4_PLAIN
@@ -442,7 +456,6 @@ def gemm_oracle(gemm: str, strategy: int, X, W, GY, *, patterns=None, r: int = D
     out["oe"] = oe
 
     a_zero_rows = a_zero_cols = b_zero_rows = b_zero_cols = None
-    side = None
     if oe is not None:
         idx = oe["idx"]
         side = "A" if SOURCES[gemm][0] == oe["source"] else "B"
@@ -451,18 +464,14 @@ def gemm_oracle(gemm: str, strategy: int, X, W, GY, *, patterns=None, r: int = D
                 a_zero_cols = idx
             else:
                 b_zero_cols = idx
-            out["a_o"] = A[:, idx].copy()           # P x r, original values
-            out["b_o"] = Bt[:, idx].copy()          # Q x r, original values (partner kept)
+            out["a_o"] = A[:, idx].copy()           # rows x r, original values
+            out["b_o"] = Bt[:, idx].copy()          # cols x r, original values (partner kept)
         elif oe["role"] == "P":
-            a_zero_rows = idx
+            a_zero_rows = np.nonzero(np.isin(rows, idx))[0]     # positions among the requested rows
         else:  # "Q"
-            b_zero_rows = idx
+            b_zero_rows = np.nonzero(np.isin(cols, idx))[0]     # positions among the requested columns
 
-    # residual of A restricted to the requested rows
-    a_rows_zero = None
-    if a_zero_rows is not None:
-        a_rows_zero = np.nonzero(np.isin(rows, a_zero_rows))[0]
-    qa = quantize_operand(A[rows], hadamard, zero_rows=a_rows_zero, zero_cols=a_zero_cols)
+    qa = quantize_operand(A, hadamard, zero_rows=a_zero_rows, zero_cols=a_zero_cols)
     qb = quantize_operand(Bt, hadamard, zero_rows=b_zero_rows, zero_cols=b_zero_cols)
     out["qa"], out["qb"] = qa, qb
     C = dequantize_operand(*qa) @ dequantize_operand(*qb).T
@@ -470,28 +479,31 @@ def gemm_oracle(gemm: str, strategy: int, X, W, GY, *, patterns=None, r: int = D
     if oe is not None:
         idx = oe["idx"]
         if oe["role"] == "J":
-            C = C + bf16_to_f32(out["a_o"][rows]).astype(np.float64) @ \
-                bf16_to_f32(out["b_o"]).astype(np.float64).T
+            C = C + bf16_to_f32(out["a_o"]).astype(np.float64) @ bf16_to_f32(out["b_o"]).astype(np.float64).T
         elif oe["role"] == "P":
-            o = bf16_to_f32(A[idx]).astype(np.float64) @ bf16_to_f32(Bt).astype(np.float64).T
-            out["o"] = o
+            A_idx, _ = gemm_operands(gemm, X, W, GY, idx, cols[:0])
+            o = bf16_to_f32(A_idx).astype(np.float64) @ bf16_to_f32(Bt).astype(np.float64).T
+            out["o"] = o                            # r x len(cols)
             pos = {int(p): i for i, p in enumerate(idx)}
             for k, p in enumerate(rows):
                 if int(p) in pos:
                     C[k, :] += o[pos[int(p)]]
         else:
-            o = bf16_to_f32(A[rows]).astype(np.float64) @ bf16_to_f32(Bt[idx]).astype(np.float64).T
-            out["o"] = o
-            C[:, idx] += o
+            _, Bt_idx = gemm_operands(gemm, X, W, GY, rows[:0], idx)
+            o = bf16_to_f32(A).astype(np.float64) @ bf16_to_f32(Bt_idx).astype(np.float64).T
+            out["o"] = o                            # len(rows) x r
+            pos = {int(q): i for i, q in enumerate(idx)}
+            for k, q in enumerate(cols):
+                if int(q) in pos:
+                    C[:, k] += o[:, pos[int(q)]]
     out["C"] = C
     return out
 
 
 def exact_product(gemm: str, X, W, GY, rows=None) -> np.ndarray:
     """A.B over the original bf16 operands in float64 (the quality reference)."""
-    A, Bt = gemm_operands(gemm, X, W, GY)
-    rows = np.arange(A.shape[0]) if rows is None else np.asarray(rows)
-    return bf16_to_f32(A[rows]).astype(np.float64) @ bf16_to_f32(Bt).astype(np.float64).T
+    A, Bt = gemm_operands(gemm, X, W, GY, None if rows is None else np.asarray(rows))
+    return bf16_to_f32(A).astype(np.float64) @ bf16_to_f32(Bt).astype(np.float64).T
 
 
 def rel_mse(C, C_exact) -> float:

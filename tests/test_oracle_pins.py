@@ -344,10 +344,19 @@ def test_gemm_quantised_close_to_exact_and_row_subset_consistent():
         exact = O.exact_product(g, X, W, GY)
         assert O.rel_mse(full["C"], exact) < 0.05, (g, strat)
         rows = np.array([0, 5, 77, full["C"].shape[0] - 1])
+        cols = np.array([1, 6, 90, full["C"].shape[1] - 1])
         if full["oe"] is not None and full["oe"]["role"] == "P":
             rows = np.concatenate([rows, full["oe"]["idx"][:3]])
+        if full["oe"] is not None and full["oe"]["role"] == "Q":
+            cols = np.concatenate([cols, full["oe"]["idx"][:3]])
         sub = O.gemm_oracle(g, strat, X, W, GY, patterns=pats, r=16, rows=rows, oe=full["oe"])
         assert np.array_equal(sub["C"], full["C"][rows]), (g, strat)
+        # a block of rows x columns: the same numbers, with only those lines quantised
+        blk = O.gemm_oracle(g, strat, X, W, GY, patterns=pats, r=16, rows=rows, cols=cols, oe=full["oe"])
+        assert np.array_equal(blk["C"], full["C"][np.ix_(rows, cols)]), (g, strat)
+    roles = {O.gemm_oracle(g, s_, X, W, GY, patterns=pats, r=16)["oe"]["role"]
+             for g, s_ in (("dgrad", O.OE_LEFT), ("wgrad", O.OE_LEFT), ("wgrad", O.OE_RIGHT))}
+    assert roles == {"P", "J", "Q"}            # outer rows, inner and outer columns all covered
 
 
 def test_outer_oe_rows_are_exact_products():
