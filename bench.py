@@ -210,16 +210,18 @@ def zero_axis(gemm: str, strategy: int, r: int, pats: dict, tensor: str) -> int:
     return axis if t == tensor else -1
 
 
-def launches_per_gemm(gemm: str, strategy: int, r: int, pats: dict, foid_shared: bool) -> int:
+def launches_per_gemm(gemm: str, strategy: int, r: int, pats: dict, foid_shared: bool,
+                      pre_gathered: bool = False) -> int:
     """Kernels the dispatcher launches for one GEMM (the launch sequence of adahop.cu)."""
     if strategy == 3:                        # BF16: one GEMM
         return 1
     if strategy in (1, 2) and r > 0:
         t, axis = oe_source(gemm, strategy, pats)
         role = _AXIS_ROLE[gemm][t][axis]
-        foid = 0 if foid_shared else 2       # local top-r + merge
-        # quantise A, B; inner: gather A_o, B_o + fused GEMM; outer: GEMM + gather + BF16 GEMM + scatter-add
-        return foid + 2 + (3 if role == "J" else 4)
+        foid = 0 if foid_shared else 1       # one launch: local top-r, the last CTA merges
+        gath = 0 if pre_gathered else 1      # this GEMM's outlier slices in one launch
+        # quantise A, B; inner: fused GEMM; outer: GEMM + BF16 outlier GEMM + scatter-add
+        return foid + 2 + gath + (1 if role == "J" else 3)
     return 3                                 # quantise A, quantise B, GEMM
 
 
@@ -243,33 +245,45 @@ class Bench:
         for c in self.cases:
             p = c.plan
             pats = {"X": p.x, "W": p.w, "GY": p.gy}
-            n += launches_per_gemm("fwd", p.fwd, p.oe_rank, pats, False)
-            n += launches_per_gemm("dgrad", p.dgrad, p.oe_rank, pats, False)
-            shared = (p.dgrad in (1, 2) and p.wgrad in (1, 2) and p.oe_rank > 0 and
-                      oe_source("dgrad", p.dgrad, pats) == oe_source("wgrad", p.wgrad, pats))
-            n += launches_per_gemm("wgrad", p.wgrad, p.oe_rank, pats, shared)
-            # prep fusion: one dual-orientation pass replaces the two quantisations of G_Y when
-            # both GEMMs quantise it with the same Hadamard setting and outlier mask
+            r = p.oe_rank
+
             def gy_mask(gemm, st):
-                if st in (1, 2) and p.oe_rank > 0:
+                if st in (1, 2) and r > 0:
                     t, axis = oe_source(gemm, st, pats)
                     return axis if t == "GY" else -1
                 return -1
-            if (p.dgrad != 3 and p.wgrad != 3 and (p.dgrad == 4) == (p.wgrad == 4)
-                    and gy_mask("dgrad", p.dgrad) == gy_mask("wgrad", p.wgrad)):
-                n -= 1
+            # prep fusion: one dual-orientation pass quantises G_Y for both backward GEMMs when they
+            # share the Hadamard setting and the outlier mask; FOID then runs once, up front, and
+            # both GEMMs' outlier slices (when they extract those lines) are gathered in one launch
+            dual = (p.dgrad != 3 and p.wgrad != 3 and (p.dgrad == 4) == (p.wgrad == 4)
+                    and gy_mask("dgrad", p.dgrad) == gy_mask("wgrad", p.wgrad))
+            foid_up = dual and gy_mask("dgrad", p.dgrad) >= 0
+            fc = ("GY", gy_mask("dgrad", p.dgrad)) if foid_up else None
+            pre = {g: foid_up and st in (1, 2) and r > 0 and oe_source(g, st, pats) == fc
+                   for g, st in (("dgrad", p.dgrad), ("wgrad", p.wgrad))}
+            n += launches_per_gemm("fwd", p.fwd, r, pats, False)
+            if foid_up:
+                n += 1 + (1 if any(pre.values()) else 0)     # FOID + the shared multi-gather
+                n += launches_per_gemm("dgrad", p.dgrad, r, pats, pre["dgrad"], pre["dgrad"])
+                n += launches_per_gemm("wgrad", p.wgrad, r, pats, pre["wgrad"], pre["wgrad"])
+            else:
+                n += launches_per_gemm("dgrad", p.dgrad, r, pats, False)
+                shared = (p.dgrad in (1, 2) and p.wgrad in (1, 2) and r > 0 and
+                          oe_source("dgrad", p.dgrad, pats) == oe_source("wgrad", p.wgrad, pats))
+                n += launches_per_gemm("wgrad", p.wgrad, r, pats, shared)
+            if dual:
+                n -= 1                               # one pass replaces the two quantisations of G_Y
             # saved context: the backward GEMMs skip quantising X (wgrad) and W (dgrad); the forward
             # call writes them, in its own quantisation pass when mask and Hadamard setting agree,
             # else in a separate pass (FOID first when the backward GEMM zeroes lines)
-            r = p.oe_rank
             for tensor, bgemm, bst in (("X", "wgrad", p.wgrad), ("W", "dgrad", p.dgrad)):
                 if bst == 3:
                     continue
                 n -= 1
                 zf, zb = zero_axis("fwd", p.fwd, r, pats, tensor), zero_axis(bgemm, bst, r, pats, tensor)
-                dual = p.fwd != 3 and zf == zb and (p.fwd != 4) == (bst != 4)
-                if not dual:
-                    n += 1 + (2 if zb >= 0 else 0)
+                dual_f = p.fwd != 3 and zf == zb and (p.fwd != 4) == (bst != 4)
+                if not dual_f:
+                    n += 1 + (1 if zb >= 0 else 0)
         return n
 
     def strategies(self) -> dict:
@@ -985,6 +999,48 @@ def profile(q, device, args):
         print(f"profiled one step: {b.launches_per_step()} launches")
         return
     from synthetic import normal_bf16
+    if args.profile == "bwd":
+        # one linear (the gate projection, N = 14336, K = 4096) through the saved-context path:
+        # a warm-up fwd + bwd, then a second one (~3 GB on the device: its tensors and workspace)
+        wl = WORKLOADS[WORKLOAD]
+        c = LinearCase(q, wl, 4, device)
+        ws = q.new_workspace(c.ws_bytes(q), device=device)
+        for _ in range(2):
+            q.adahop_linear_fwd_save(c.plan, c.X, c.W, c.Y, c.saved, ws)
+            q.adahop_linear_bwd_saved(c.plan, c.GY, c.X, c.W, c.saved, c.dX, c.dW, ws)
+        torch.cuda.synchronize()
+        assert q.adahop_get_device_status(ws) == 0
+        print("profiled two fwd + bwd passes of the gate projection")
+        return
+    if args.profile == "gemms":
+        # the fused GEMM on each of the step's 21 shapes, one shape's operands on the device at a
+        # time (at most ~1.5 GB), two launches each (for a one-pass DRAM-byte capture per launch)
+        wl = WORKLOADS[WORKLOAD]
+        ws = q.new_workspace(4096, device=device)
+        n = 0
+        for lin in wl.linears:
+            M, N, K = wl.M, lin.N, lin.K
+            for gemm, (P, Q, J, r) in (("fwd", (M, N, K, 0)), ("dgrad", (M, K, N, 0)), ("wgrad", (N, K, M, 64))):
+                A = normal_bf16(P, J, 1.0, 1, device=device)
+                B = normal_bf16(Q, J, 0.02, 2, device=device)
+                ac = torch.empty(P * J // 2, dtype=torch.uint8, device=device)
+                asf = torch.empty(P * J // 32, dtype=torch.uint8, device=device)
+                bc = torch.empty(Q * J // 2, dtype=torch.uint8, device=device)
+                bsf = torch.empty(Q * J // 32, dtype=torch.uint8, device=device)
+                q.adahop_quantize_mxfp4(A, 1, 1, None, None, ac, asf, 1)
+                q.adahop_quantize_mxfp4(B, 1, 1, None, None, bc, bsf, 1)
+                del A, B
+                Ao = torch.randn((P, r), device=device).to(torch.bfloat16) if r else None
+                Bo = torch.randn((Q, r), device=device).to(torch.bfloat16) if r else None
+                C = torch.empty((P, Q), dtype=torch.bfloat16, device=device)
+                for _ in range(2):
+                    q.adahop_gemm_mxfp4(ac, asf, bc, bsf, P, Q, J, Ao, Bo, r, C, ws)
+                    n += 1
+                torch.cuda.synchronize()
+                del ac, asf, bc, bsf, Ao, Bo, C
+        assert q.adahop_get_device_status(ws) == 0
+        print(f"profiled {n} fused MXFP4 GEMM launches (the step's 21 shapes, two each)")
+        return
     if args.profile == "foid":
         M, N, r = 32768, 14336, 64                      # row probe of the gate G_Y (dgrad / wgrad OE)
         G = normal_bf16(M, N, 1e-3, 3, outlier_axis="row", outlier_count=64, outlier_scale=40.0, device=device)
@@ -1081,11 +1137,14 @@ def main():
                     help="split-K sweep of the outer-OE outlier GEMM on the step's shapes; prints one JSON object")
     ap.add_argument("--quality", action="store_true",
                     help="relative MSE of the Table 3 plans on the 8B gate projection; prints one JSON object")
-    ap.add_argument("--profile", choices=["step", "gemm", "quant", "quant1", "foid", "scatter", "bf16", "outlier"],
+    ap.add_argument("--profile", choices=["step", "bwd", "gemm", "gemms", "quant", "quant1", "foid", "scatter",
+                                          "bf16", "outlier"],
                     default=None,
                     help="for ncu only (prints no bench line): 'step' = warm-up steps then one step "
-                         "of the workload; 'gemm' = three launches of the fused MXFP4 GEMM on the "
-                         "dgrad shape P=32768, Q=4096, J=14336; 'quant' = three launches of the "
+                         "of the workload; 'bwd' = two fwd + bwd passes of the gate projection alone; "
+                         "'gemm' = three launches of the fused MXFP4 GEMM on the "
+                         "dgrad shape P=32768, Q=4096, J=14336; 'gemms' = two launches of it on each of the "
+                         "step's 21 shapes, one shape's operands at a time; 'quant' = three launches of the "
                          "dual-orientation quantiser on the 32768 x 14336 G_Y; 'quant1' = three rows- "
                          "and three cols-orientation launches on it; 'foid' = three row FOID calls on it "
                          "(r = 64); 'scatter' = three scatter-adds of 64 rows into 32768 x 4096; 'bf16' = "

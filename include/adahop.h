@@ -22,9 +22,9 @@
  *     allocates no device memory: scratch lives in the caller's workspace.
  *   - Every call is asynchronous on the given CUDA stream (NULL = legacy default stream)
  *     unless documented as synchronous.  Host-side argument errors return before any launch.
- *   - Shapes: M, N, K must be positive multiples of 128.  OE rank r: 0 <= r <= 256, a multiple
- *     of 8, and r <= the number of lines it is drawn from.  Device pointers must be 16-byte
- *     aligned and the workspace 256-byte aligned; otherwise ADAHOP_ERR_ALIGN.
+ *   - Shapes: M, N, K must be positive multiples of 128.  OE rank r: 0 <= r <= 256 and r <= the
+ *     number of lines it is drawn from.  Device pointers must be 16-byte aligned and the
+ *     workspace 256-byte aligned; otherwise ADAHOP_ERR_ALIGN.
  *   - Inputs must be finite; results for NaN/Inf inputs are unspecified.
  *   - A workspace must start with its first 256 bytes zeroed (the status word lives there).
  *     A device-side failure (a bounded wait that ran out) is recorded in that status word;
@@ -114,14 +114,14 @@ adahop_status adahop_calibrate(const void *X, const void *W, const void *GY, int
 
 /* Forward GEMM Y = X.W^T (M x N) with plan->fwd.  out_dtype selects bf16 or fp32 Y. */
 adahop_status adahop_linear_fwd(const adahop_plan *plan, const void *X, const void *W,
-                                int64_t M, int64_t N, int64_t K, void *Y, int out_dtype,
+                                int64_t M, int64_t N, int64_t K, void *Y, adahop_out_dtype out_dtype,
                                 void *workspace, size_t ws_bytes, adahop_stream_t stream);
 
 /* Backward GEMMs dX = G_Y.W (M x K) with plan->dgrad and dW = G_Y^T.X (N x K) with
  * plan->wgrad.  Either output may be NULL to skip that GEMM. */
 adahop_status adahop_linear_bwd(const adahop_plan *plan, const void *GY, const void *X,
                                 const void *W, int64_t M, int64_t N, int64_t K, void *dX,
-                                void *dW, int out_dtype, void *workspace, size_t ws_bytes,
+                                void *dW, adahop_out_dtype out_dtype, void *workspace, size_t ws_bytes,
                                 adahop_stream_t stream);
 
 /* Saved context (AdaHOP appendix, IHT and Quantization: the forward pass saves quantised
@@ -145,7 +145,7 @@ adahop_status adahop_saved_size(const adahop_plan *plan, int64_t M, int64_t N, i
  * bytes (may be NULL only when that size is 0); ADAHOP_ERR_WORKSPACE if saved_bytes is short.
  * The buffer must stay untouched until the matching adahop_linear_bwd_saved has run. */
 adahop_status adahop_linear_fwd_save(const adahop_plan *plan, const void *X, const void *W,
-                                     int64_t M, int64_t N, int64_t K, void *Y, int out_dtype,
+                                     int64_t M, int64_t N, int64_t K, void *Y, adahop_out_dtype out_dtype,
                                      void *saved, size_t saved_bytes, void *workspace,
                                      size_t ws_bytes, adahop_stream_t stream);
 
@@ -154,7 +154,7 @@ adahop_status adahop_linear_fwd_save(const adahop_plan *plan, const void *X, con
 adahop_status adahop_linear_bwd_saved(const adahop_plan *plan, const void *GY, const void *X,
                                       const void *W, const void *saved, size_t saved_bytes,
                                       int64_t M, int64_t N, int64_t K, void *dX, void *dW,
-                                      int out_dtype, void *workspace, size_t ws_bytes,
+                                      adahop_out_dtype out_dtype, void *workspace, size_t ws_bytes,
                                       adahop_stream_t stream);
 
 /* Waits for the stream, then reads (and clears) the workspace status word.
@@ -181,7 +181,10 @@ adahop_status adahop_check_bounded_wait(void *workspace, size_t ws_bytes, adahop
  * Score = float32 population variance of the probe (fixed pairwise summation tree, no FMA);
  * idx_out (device, int32[r]) receives the r best lines in ascending order, ties to the lower
  * index.  line_mask_out (device, may be NULL) receives a bitmap of ceil(lines/32) uint32 words
- * with the selected lines set.  Needs adahop_foid_workspace_size() bytes of workspace. */
+ * with the selected lines set.  One kernel launch: the CTA that finishes the per-chunk ranking
+ * last merges the chunks.  Needs adahop_foid_workspace_size() bytes of workspace, 256-byte
+ * aligned, whose first 256 bytes are zero at the first call (a completion counter; every call
+ * leaves it zero again, so a workspace can be reused without clearing). */
 adahop_status adahop_foid(const void *T, int64_t rows, int64_t cols, int axis, int r,
                           int32_t *idx_out, uint32_t *line_mask_out, void *workspace,
                           size_t ws_bytes, adahop_stream_t stream);
@@ -192,15 +195,21 @@ size_t adahop_foid_workspace_size(int64_t lines, int r);
  * (a plug-in or callback inside another runtime that owns all device memory) or that must not
  * call cudaMalloc (it may synchronise the device and can fail at run time).  It computes exactly
  * what adahop_foid computes (same arguments and results, minus the workspace) and allocates
- * nothing: its scratch is a fixed 64 KB device array inside the library (8192 candidate keys),
- * held by every GPU that loads the library until the process exits.
+ * nothing: its scratch is a fixed 64.25 KB device array inside the library (a 256-byte counter
+ * header and 8192 candidate keys), held by every GPU that loads the library until the process
+ * exits.
  *   - Limit: ceil(lines / 2048) * r must be <= 8192 (e.g. r = 256 for up to 65536 lines);
  *     larger requests return ADAHOP_ERR_SHAPE before anything is launched.
- *   - The first call on a device looks up the array's device address (once per device, with
- *     that device current); make that first call before any stream capture.
- *   - All calls share the array and it keeps the last call's contents (nothing in it needs to
- *     start at zero).  Calls whose kernels overlap on the GPU (e.g. on different streams) race
- *     on it and must be serialised by the caller. */
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and keeps it for that device's context; after a device reset (a new context) the
+ *     next call looks it up again.  Under CUDA's lazy module loading that first lookup may load
+ *     the library's device code and allocate its device globals (this array among them) at that
+ *     moment, and may synchronise: make the first call on each device before any stream capture
+ *     and at a point where that one-time set-up is acceptable.  Later calls allocate nothing.
+ *   - All calls share the array and it keeps the last call's contents.  The one part that must
+ *     start at zero, the counter, is zero when the library loads and every call leaves it zero;
+ *     the candidate slots are written before they are read.  Calls whose kernels overlap on the
+ *     GPU (e.g. on different streams) race on it and must be serialised by the caller. */
 adahop_status adahop_foid_noalloc(const void *T, int64_t rows, int64_t cols, int axis, int r,
                                   int32_t *idx_out, uint32_t *line_mask_out,
                                   adahop_stream_t stream);
@@ -256,7 +265,7 @@ adahop_status adahop_gather(const void *T, int64_t rows, int64_t cols, const int
 adahop_status adahop_gemm_mxfp4(const uint8_t *a_codes, const uint8_t *a_scales,
                                 const uint8_t *b_codes, const uint8_t *b_scales, int64_t P,
                                 int64_t Q, int64_t J, const void *A_o, const void *B_o, int r,
-                                void *C, int out_dtype, void *workspace, size_t ws_bytes,
+                                void *C, adahop_out_dtype out_dtype, void *workspace, size_t ws_bytes,
                                 adahop_stream_t stream);
 
 /* BF16 GEMM C (P x Q) = A . B, float32 accumulation (Fig. 5's BF16 path; also the outlier
@@ -267,15 +276,30 @@ adahop_status adahop_gemm_mxfp4(const uint8_t *a_codes, const uint8_t *a_scales,
  * c_partial).  P >= 1 (a multiple of 64 when A is
  * stored J x P); Q and J multiples of 64.  The workspace only carries the status word. */
 adahop_status adahop_gemm_bf16(const void *A, int a_kmajor, const void *B, int b_kmajor,
-                               int64_t P, int64_t Q, int64_t J, void *C, int out_dtype,
+                               int64_t P, int64_t Q, int64_t J, void *C, adahop_out_dtype out_dtype,
                                int splits, float *c_partial, void *workspace, size_t ws_bytes,
                                adahop_stream_t stream);
+
+/* Outlier GEMM of outer OE with the scatter-add fused (appendix, Fused Scatter-Add: the outlier
+ * product is added in place, without materialising it).  O = A . B with A and B stored as in
+ * adahop_gemm_bf16 (a_kmajor / b_kmajor); then
+ *   axis 0 (P = r):  C[idx[i], q] += O[i, q]   for i < r, q < Q  (Q = c_cols)
+ *   axis 1 (Q = r):  C[p, idx[i]] += O[p, i]   for p < P, i < r  (P = c_rows)
+ * C: c_rows x c_cols, bf16 or fp32 per out_dtype, read and written in place; each sum is formed
+ * in float32 (the J range split over the CTAs of a cluster, partials summed in a fixed order),
+ * added to C's value in float32 and rounded once to C's type.  Indices outside C are skipped.
+ * One kernel launch.  1 <= r <= 256; J a multiple of 64; c_cols a multiple of 8; P (Q) a multiple
+ * of 64 when A (B) is stored J-major.  The workspace only carries the status word (>= 256 bytes). */
+adahop_status adahop_gemm_bf16_scatter_add(const void *A, int a_kmajor, const void *B, int b_kmajor, int64_t P,
+                                           int64_t Q, int64_t J, void *C, int64_t c_rows, int64_t c_cols,
+                                           adahop_out_dtype out_dtype, const int32_t *idx, int r, int axis, void *workspace,
+                                           size_t ws_bytes, adahop_stream_t stream);
 
 /* Fused scatter-add (appendix, Fused Scatter-Add): adds the outlier product in place.
  * partial: fp32, splits x r x Q (axis 0) or splits x P x r (axis 1), summed over splits.
  * axis 0: C[idx[i], q] += sum_s partial[s, i, q];  axis 1: C[p, idx[i]] += sum_s partial[s, p, i].
  * The sum is formed in float32 and rounded once to C's type. */
-adahop_status adahop_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype,
+adahop_status adahop_scatter_add(void *C, int64_t P, int64_t Q, adahop_out_dtype out_dtype,
                                  const float *partial, int splits, const int32_t *idx, int r,
                                  int axis, adahop_stream_t stream);
 

@@ -67,6 +67,9 @@ PROTOTYPES = {
                                   c_size_t, c_void_p]),
     "adahop_gemm_bf16": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int64, c_int64, c_int64,
                                  c_void_p, c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "adahop_gemm_bf16_scatter_add": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int64, c_int64, c_int64,
+                                             c_void_p, c_int64, c_int64, c_int, c_void_p, c_int, c_int,
+                                             c_void_p, c_size_t, c_void_p]),
     "adahop_scatter_add": (c_int, [c_void_p, c_int64, c_int64, c_int, c_void_p, c_int, c_void_p,
                                    c_int, c_int, c_void_p]),
     "adahop_calibration_stats": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_void_p,

@@ -257,6 +257,14 @@ def adahop_gemm_bf16(A, a_kmajor: int, B, b_kmajor: int, P: int, Q: int, J: int,
            "adahop_gemm_bf16")
 
 
+def adahop_gemm_bf16_scatter_add(A, a_kmajor: int, B, b_kmajor: int, P: int, Q: int, J: int, C_out, idx,
+                                 r: int, axis: int, workspace, stream=None) -> None:
+    c_rows, c_cols = C_out.shape
+    _check(LIB.adahop_gemm_bf16_scatter_add(_p(A), a_kmajor, _p(B), b_kmajor, P, Q, J, _p(C_out), c_rows, c_cols,
+                                            _out_dtype(C_out), _p(idx), r, axis, _p(workspace), workspace.numel(),
+                                            _stream(stream)), "adahop_gemm_bf16_scatter_add")
+
+
 def adahop_scatter_add(C_out, partial, splits: int, idx, r: int, axis: int, stream=None) -> None:
     P, Q = C_out.shape
     _check(LIB.adahop_scatter_add(_p(C_out), P, Q, _out_dtype(C_out), _p(partial), splits, _p(idx), r, axis,

@@ -102,9 +102,11 @@ adahop_status make_map(CUtensorMap *map, CUtensorMapDataType dt, size_t elem_byt
 
 // ------------------------------------------------------------------------- validation
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-bool dim_ok(int64_t d) { return d > 0 && d % 128 == 0 && d <= (int64_t(1) << 31); }
+// the GEMMs carry tile coordinates in int32 (TMA coordinates are signed 32-bit)
+bool dim_ok(int64_t d) { return d > 0 && d % 128 == 0 && d < (int64_t(1) << 31); }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+int round8(int r) { return (r + 7) & ~7; }
 
 // ------------------------------------------------------------------------- workspace layout
 // One GEMM's scratch.  The region sizes are upper bounds over all strategies.
@@ -140,8 +142,8 @@ GemmWs gemm_ws(int64_t P, int64_t Q, int64_t J, int r, int num_sms, int64_t line
   w.a_sf = take(static_cast<size_t>(P * J / 32));
   w.b_codes = take(static_cast<size_t>(Q * J / 2));
   w.b_sf = take(static_cast<size_t>(Q * J / 32));
-  w.ao = take(static_cast<size_t>(P) * rr * 2);
-  w.bo = take(static_cast<size_t>(Q) * rr * 2);
+  w.ao = take(static_cast<size_t>(P) * round8(rr) * 2);
+  w.bo = take(static_cast<size_t>(Q) * round8(rr) * 2);
   w.gath = take(static_cast<size_t>(rr) * J * 2);
   // outlier GEMM partials: rows case r x Q per split, cols case P x r per split
   const int64_t k_stages = (J + 63) / 64;
@@ -219,12 +221,17 @@ OeChoice oe_choice(int gemm, int strategy, const int pats[3]) {
   return c;
 }
 
+// Inside the workspace's zeroed first 256 bytes: the status word at offset 0 and FOID's completion
+// counter (zero whenever no FOID launch is running: every launch leaves it zero).
+constexpr size_t kFoidCounterOffset = 64;
+
 struct Ctx {
   cudaStream_t s;
   uint8_t *ws;
   GemmWs lay;
   int num_sms;
   uint32_t *status() const { return reinterpret_cast<uint32_t *>(ws + lay.status); }
+  uint32_t *foid_counter() const { return reinterpret_cast<uint32_t *>(ws + lay.status + kFoidCounterOffset); }
 };
 
 adahop_status bf16_gemm(const Ctx &cx, const void *A, int a_kmajor, const void *B, int b_kmajor,
@@ -254,6 +261,40 @@ adahop_status bf16_gemm(const Ctx &cx, const void *A, int a_kmajor, const void *
   g.c_partial = partial;
   g.status = cx.status();
   CUDA_TRY(launch_gemm(g, maps, cx.num_sms, cx.s), "bf16 gemm launch");
+  return ADAHOP_OK;
+}
+
+// Outer-OE outlier product with the scatter-add fused: C[idx, :] += A . B (axis 0, P = r) or
+// C[:, idx] += A . B (axis 1, Q = r); C is c_rows x c_cols.  One launch (a cluster split-K GEMM).
+adahop_status bf16_scatter_gemm(const Ctx &cx, const void *A, int a_kmajor, const void *B, int b_kmajor, int64_t P,
+                                int64_t Q, int64_t J, void *C, int64_t c_rows, int64_t c_cols, int out_dtype,
+                                const int32_t *idx, int axis) {
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  if (a_kmajor)
+    ST_TRY(make_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, J, P, 64, 128));
+  else
+    ST_TRY(make_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, P, J, 64, 64));
+  if (b_kmajor)
+    ST_TRY(make_map(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, J, Q, 64, 256));
+  else
+    ST_TRY(make_map(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, Q, J, 64, 64));
+  maps.ao = maps.a;
+  maps.bo = maps.b;
+  GemmArgs g{};
+  g.P = P; g.Q = Q; g.J = J;
+  g.kind = 2;
+  g.a_mn_major = !a_kmajor;
+  g.b_mn_major = !b_kmajor;
+  g.C = C;
+  g.out_dtype = out_dtype;
+  g.splits = 1;
+  g.status = cx.status();
+  g.scatter_idx = idx;
+  g.scatter_axis = axis;
+  g.c_rows = c_rows;
+  g.c_cols = c_cols;
+  CUDA_TRY(launch_gemm(g, maps, cx.num_sms, cx.s), "bf16 outlier gemm (scatter-add) launch");
   return ADAHOP_OK;
 }
 
@@ -309,6 +350,33 @@ struct PreA {
   uint8_t *codes, *sf;
 };
 
+// Outlier slices of one GEMM already gathered (one launch for both backward GEMMs): ao / bo
+// for inner OE, gath for outer OE.
+struct PreGath {
+  uint16_t *ao, *bo, *gath;
+};
+
+// The gathers one OE GEMM needs (0, 1 or 2 jobs) into ao / bo / gath; returns the job count.
+int oe_gather_jobs(int gemm, const OeChoice &oe, const Tensor t[3], const int32_t *idx, int r, const PreGath &dst,
+                   GatherJob *jobs) {
+  const GemmRoles ro = roles_of(gemm);
+  const Tensor &ta = t[ro.a_src];
+  const Tensor &tb = t[ro.b_src];
+  if (oe.role == 'J') {
+    // r8 columns per slice line, the last r8 - r of them +0 (they add nothing to the product): the
+    // fused GEMM loads slices whose rows are a multiple of 16 bytes
+    jobs[0] = GatherJob{ta.p, ta.rows, ta.cols, idx, r, ro.a_inner_axis == 1 ? 1 : 2, dst.ao, round8(r)};
+    jobs[1] = GatherJob{tb.p, tb.rows, tb.cols, idx, r, ro.b_inner_axis == 1 ? 1 : 2, dst.bo, round8(r)};
+    return 2;
+  }
+  if (oe.role == 'P') {
+    jobs[0] = GatherJob{ta.p, ta.rows, ta.cols, idx, r, ro.a_inner_axis == 1 ? 0 : 3, dst.gath, 0};
+    return 1;
+  }
+  jobs[0] = GatherJob{tb.p, tb.rows, tb.cols, idx, r, ro.b_inner_axis == 1 ? 0 : 3, dst.gath, 0};
+  return 1;
+}
+
 // pre_a / pre_b: operand already quantised in this GEMM's orientation (codes + tensor-core
 // scales), so its quantisation is skipped.  alt_a / alt_b: the operand is quantised by the
 // dual-orientation pass, which also writes its other orientation (J = the stored rows) there;
@@ -316,7 +384,8 @@ struct PreA {
 adahop_status run_gemm(const Ctx &cx, int gemm, int strategy, int r, const Tensor t[3],
                        const int pats[3], void *C, int out_dtype, FoidCache *fc,
                        const PreA *pre_a = nullptr, const PreA *pre_b = nullptr,
-                       const PreA *alt_a = nullptr, const PreA *alt_b = nullptr) {
+                       const PreA *alt_a = nullptr, const PreA *alt_b = nullptr,
+                       const PreGath *pre_g = nullptr) {
   const GemmShape sh = shape_of(gemm, t[T_X].rows, t[T_W].rows, t[T_X].cols);
   const GemmRoles ro = roles_of(gemm);
   const Tensor &ta = t[ro.a_src];
@@ -336,7 +405,7 @@ adahop_status run_gemm(const Ctx &cx, int gemm, int strategy, int r, const Tenso
     const Tensor &src = t[oe.tensor];
     const bool cached = fc && fc->tensor == oe.tensor && fc->axis == oe.axis && fc->r == r;
     if (!cached) {
-      CUDA_TRY(launch_foid(src.p, src.rows, src.cols, oe.axis, r, idx, mask, ws + cx.lay.foid, cx.s),
+      CUDA_TRY(launch_foid(src.p, src.rows, src.cols, oe.axis, r, idx, mask, ws + cx.lay.foid, cx.foid_counter(), cx.s),
                "foid");
       if (fc) *fc = FoidCache{oe.tensor, oe.axis, r};
     }
@@ -374,34 +443,24 @@ adahop_status run_gemm(const Ctx &cx, int gemm, int strategy, int r, const Tenso
   }
   if (oe.tensor < 0) return mxf4_gemm(cx, ac, asf, bc, bsf, sh.P, sh.Q, sh.J, nullptr, nullptr, 0, C, out_dtype);
 
-  uint16_t *ao = reinterpret_cast<uint16_t *>(ws + cx.lay.ao);
-  uint16_t *bo = reinterpret_cast<uint16_t *>(ws + cx.lay.bo);
-  uint16_t *gath = reinterpret_cast<uint16_t *>(ws + cx.lay.gath);
-  float *partial = reinterpret_cast<float *>(ws + cx.lay.partial);
+  const PreGath own{reinterpret_cast<uint16_t *>(ws + cx.lay.ao), reinterpret_cast<uint16_t *>(ws + cx.lay.bo),
+                    reinterpret_cast<uint16_t *>(ws + cx.lay.gath)};
+  const PreGath &g = pre_g ? *pre_g : own;
+  if (!pre_g) {
+    // one launch for this GEMM's outlier slices (A_o and B_o, or the outer lines)
+    GatherJob jobs[2];
+    const int n = oe_gather_jobs(gemm, oe, t, idx, r, own, jobs);
+    CUDA_TRY(launch_gathers(jobs, n, cx.s), "gather outlier slices");
+  }
   if (oe.role == 'J') {
     // inner: A_o[p, i] = A[p, idx[i]], B_o[q, i] = B^T[q, idx[i]] from the original bf16 values
-    CUDA_TRY(launch_gather(ta.p, ta.rows, ta.cols, idx, r, ro.a_inner_axis == 1 ? 1 : 2, ao, cx.s), "gather A_o");
-    CUDA_TRY(launch_gather(tb.p, tb.rows, tb.cols, idx, r, ro.b_inner_axis == 1 ? 1 : 2, bo, cx.s), "gather B_o");
-    return mxf4_gemm(cx, ac, asf, bc, bsf, sh.P, sh.Q, sh.J, ao, bo, r, C, out_dtype);
+    return mxf4_gemm(cx, ac, asf, bc, bsf, sh.P, sh.Q, sh.J, g.ao, g.bo, round8(r), C, out_dtype);
   }
   ST_TRY(mxf4_gemm(cx, ac, asf, bc, bsf, sh.P, sh.Q, sh.J, nullptr, nullptr, 0, C, out_dtype));
-  const int64_t k_stages = (sh.J + 63) / 64;
-  if (oe.role == 'P') {
-    // outer rows: O = A[idx, :] . B  (r x Q), then C[idx, :] += O
-    CUDA_TRY(launch_gather(ta.p, ta.rows, ta.cols, idx, r, ro.a_inner_axis == 1 ? 0 : 3, gath, cx.s),
-             "gather outlier rows");
-    const int splits = choose_splits((sh.Q + 255) / 256, k_stages, cx.num_sms);
-    ST_TRY(bf16_gemm(cx, gath, 1, tb.p, ro.b_kmajor, r, sh.Q, sh.J, nullptr, 1, splits, partial));
-    CUDA_TRY(launch_scatter_add(C, sh.P, sh.Q, out_dtype, partial, splits, idx, r, 0, cx.s), "scatter-add");
-  } else {
-    // outer cols: O = A . B[:, idx]  (P x r), then C[:, idx] += O
-    CUDA_TRY(launch_gather(tb.p, tb.rows, tb.cols, idx, r, ro.b_inner_axis == 1 ? 0 : 3, gath, cx.s),
-             "gather outlier cols");
-    const int splits = choose_splits((sh.P + 127) / 128, k_stages, cx.num_sms);
-    ST_TRY(bf16_gemm(cx, ta.p, ro.a_kmajor, gath, 1, sh.P, r, sh.J, nullptr, 1, splits, partial));
-    CUDA_TRY(launch_scatter_add(C, sh.P, sh.Q, out_dtype, partial, splits, idx, r, 1, cx.s), "scatter-add");
-  }
-  return ADAHOP_OK;
+  if (oe.role == 'P')   // outer rows: C[idx, :] += A[idx, :] . B  (r x Q)
+    return bf16_scatter_gemm(cx, g.gath, 1, tb.p, ro.b_kmajor, r, sh.Q, sh.J, C, sh.P, sh.Q, out_dtype, idx, 0);
+  // outer cols: C[:, idx] += A . B[:, idx]  (P x r)
+  return bf16_scatter_gemm(cx, ta.p, ro.a_kmajor, g.gath, 1, sh.P, r, sh.J, C, sh.P, sh.Q, out_dtype, idx, 1);
 }
 
 adahop_status check_plan(const adahop_plan *plan) {
@@ -412,7 +471,7 @@ adahop_status check_plan(const adahop_plan *plan) {
   const int strats[3] = {plan->fwd, plan->dgrad, plan->wgrad};
   for (int s : strats)
     if (s < 0 || s > 4) return ADAHOP_ERR_INVALID_ARG;
-  if (plan->oe_rank < 0 || plan->oe_rank > kMaxRank || (plan->oe_rank % 8) != 0) return ADAHOP_ERR_SHAPE;
+  if (plan->oe_rank < 0 || plan->oe_rank > kMaxRank) return ADAHOP_ERR_SHAPE;
   return ADAHOP_OK;
 }
 
@@ -430,6 +489,36 @@ size_t bwd_alt_offset(int64_t M, int64_t N, int64_t K, int r) {
                            gemm_ws(shw.P, shw.Q, shw.J, r, kSizingSms, lines).total));
 }
 
+// Region for the outlier slices both backward GEMMs gather in one launch: after G_Y's second
+// orientation; per GEMM (P + Q + J) x r bf16 (A_o P x r, B_o Q x r, outer lines r x J).
+size_t bwd_gath_offset(int64_t M, int64_t N, int64_t K, int r) {
+  return bwd_alt_offset(M, N, K, r) + align256(static_cast<size_t>(M * N / 2)) + align256(static_cast<size_t>(M * N / 32));
+}
+struct BwdGath {
+  size_t ao[2], bo[2], gath[2];   // offsets for dgrad, wgrad
+  size_t end;
+  PreGath at(uint8_t *ws, int k) const {
+    return PreGath{reinterpret_cast<uint16_t *>(ws + ao[k]), reinterpret_cast<uint16_t *>(ws + bo[k]),
+                   reinterpret_cast<uint16_t *>(ws + gath[k])};
+  }
+};
+BwdGath bwd_gath_layout(int64_t M, int64_t N, int64_t K, int r) {
+  BwdGath b{};
+  size_t off = bwd_gath_offset(M, N, K, r);
+  const size_t rr = static_cast<size_t>(round8(std::max(r, 1)));
+  for (int k = 0; k < 2; ++k) {
+    const GemmShape sh = shape_of(k + 1, M, N, K);
+    b.ao[k] = off;
+    off += align256(static_cast<size_t>(sh.P) * rr * 2);
+    b.bo[k] = off;
+    off += align256(static_cast<size_t>(sh.Q) * rr * 2);
+    b.gath[k] = off;
+    off += align256(static_cast<size_t>(sh.J) * rr * 2);
+  }
+  b.end = off;
+  return b;
+}
+
 size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
   size_t b = 0;
   const int64_t lines = std::max(std::max(M, N), K);
@@ -437,8 +526,7 @@ size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
     const GemmShape sh = shape_of(g, M, N, K);
     b = std::max(b, gemm_ws(sh.P, sh.Q, sh.J, r, kSizingSms, lines).total);
   }
-  b = std::max(b, bwd_alt_offset(M, N, K, r) + align256(static_cast<size_t>(M * N / 2)) +
-                      align256(static_cast<size_t>(M * N / 32)));
+  b = std::max(b, bwd_gath_layout(M, N, K, r).end);
   // calibration statistics: rows + cols floats of the largest tensor
   b = std::max(b, align256(256 + sizeof(float) * static_cast<size_t>(std::max(M, N) + std::max(N, K)) + 256));
   return b;
@@ -539,7 +627,7 @@ adahop_status quantise_saved(const Ctx &cx, const Tensor &src, int zaxis, int r,
   uint32_t *mask = reinterpret_cast<uint32_t *>(cx.ws + cx.lay.mask);
   if (zaxis >= 0)
     CUDA_TRY(launch_foid(src.p, src.rows, src.cols, zaxis, r, reinterpret_cast<int32_t *>(cx.ws + cx.lay.idx), mask,
-                         cx.ws + cx.lay.foid, cx.s),
+                         cx.ws + cx.lay.foid, cx.foid_counter(), cx.s),
              "foid");
   QuantArgs q{};
   q.T = src.p; q.rows = src.rows; q.cols = src.cols;
@@ -585,7 +673,7 @@ adahop_status linear_bwd_impl(const adahop_plan *plan, const void *GY, const voi
       uint32_t *mask = reinterpret_cast<uint32_t *>(ws + ld.mask);
       if (gmask_d >= 0) {
         CUDA_TRY(launch_foid(t[T_GY].p, M, N, gmask_d, r, reinterpret_cast<int32_t *>(ws + ld.idx), mask,
-                             ws + ld.foid, s),
+                             ws + ld.foid, reinterpret_cast<uint32_t *>(ws + kFoidCounterOffset), s),
                  "foid");
         fc = FoidCache{T_GY, gmask_d, r};
       }
@@ -602,18 +690,42 @@ adahop_status linear_bwd_impl(const adahop_plan *plan, const void *GY, const voi
       CUDA_TRY(launch_quant_dual(q, pre_w.codes, pre_w.sf, s), "quantise G_Y (both orientations)");
     }
   }
+  // Outlier slices of both GEMMs in one launch, when both extract the lines the shared FOID found
+  // (each GEMM's own gathers otherwise).
+  PreGath pg[2]{};
+  bool pre_gath[2] = {false, false};
+  if (fc.tensor >= 0) {
+    const BwdGath bl = bwd_gath_layout(M, N, K, plan->oe_rank);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int32_t *idx = reinterpret_cast<const int32_t *>(ws + ld.idx);
+    GatherJob jobs[4];
+    int n = 0;
+    const int strat[2] = {plan->dgrad, plan->wgrad};
+    void *const outs[2] = {dX, dW};
+    for (int k = 0; k < 2; ++k) {
+      if (!outs[k] || (strat[k] != ADAHOP_OE_LEFT && strat[k] != ADAHOP_OE_RIGHT) || plan->oe_rank <= 0) continue;
+      const OeChoice oe = oe_choice(k + 1, strat[k], pats);
+      if (oe.tensor != fc.tensor || oe.axis != fc.axis) continue;
+      pg[k] = bl.at(ws, k);
+      pre_gath[k] = true;
+      n += oe_gather_jobs(k + 1, oe, t, idx, plan->oe_rank, pg[k], jobs + n);
+    }
+    CUDA_TRY(launch_gathers(jobs, n, s), "gather outlier slices (both backward GEMMs)");
+  }
   const SavedLayout sl = saved ? saved_layout(plan, M, N, K) : SavedLayout{};
   uint8_t *sv = const_cast<uint8_t *>(saved);
   const PreA saved_w{sv + sl.w_codes, sv + sl.w_sf}, saved_x{sv + sl.x_codes, sv + sl.x_sf};
   if (dX) {
     Ctx cx{s, static_cast<uint8_t *>(workspace), ld, di.num_sms};
     ST_TRY(run_gemm(cx, 1, plan->dgrad, plan->oe_rank, t, pats, dX, out_dtype, share ? &fc : nullptr,
-                    dual ? &pre_d : nullptr, sl.has_w ? &saved_w : nullptr));
+                    dual ? &pre_d : nullptr, sl.has_w ? &saved_w : nullptr, nullptr, nullptr,
+                    pre_gath[0] ? &pg[0] : nullptr));
   }
   if (dW) {
     Ctx cx{s, static_cast<uint8_t *>(workspace), lw, di.num_sms};
     ST_TRY(run_gemm(cx, 2, plan->wgrad, plan->oe_rank, t, pats, dW, out_dtype, share ? &fc : nullptr,
-                    dual ? &pre_w : nullptr, sl.has_x ? &saved_x : nullptr));
+                    dual ? &pre_w : nullptr, sl.has_x ? &saved_x : nullptr, nullptr, nullptr,
+                    pre_gath[1] ? &pg[1] : nullptr));
   }
   return ADAHOP_OK;
 }
@@ -661,7 +773,7 @@ adahop_status adahop_calibrate(const void *X, const void *W, const void *GY, int
   adahop_options o;
   adahop_default_options(&o);
   if (opt) o = *opt;
-  if (!(o.tau > 0) || o.probe_len != 64 || o.oe_rank < 0 || o.oe_rank > kMaxRank || o.oe_rank % 8)
+  if (!(o.tau > 0) || o.probe_len != 64 || o.oe_rank < 0 || o.oe_rank > kMaxRank)
     return ADAHOP_ERR_INVALID_ARG;
   ST_TRY(check_shapes(M, N, K));
   if (!aligned(X, 16) || !aligned(W, 16) || (GY && !aligned(GY, 16)) || !aligned(workspace, 256))
@@ -687,7 +799,7 @@ adahop_status adahop_calibrate(const void *X, const void *W, const void *GY, int
 }
 
 adahop_status adahop_linear_fwd(const adahop_plan *plan, const void *X, const void *W, int64_t M, int64_t N,
-                                int64_t K, void *Y, int out_dtype, void *workspace, size_t ws_bytes,
+                                int64_t K, void *Y, adahop_out_dtype out_dtype, void *workspace, size_t ws_bytes,
                                 adahop_stream_t stream) {
   if (!X || !W || !Y) return ADAHOP_ERR_INVALID_ARG;
   if (out_dtype != ADAHOP_OUT_BF16 && out_dtype != ADAHOP_OUT_FP32) return ADAHOP_ERR_INVALID_ARG;
@@ -703,7 +815,7 @@ adahop_status adahop_linear_fwd(const adahop_plan *plan, const void *X, const vo
 }
 
 adahop_status adahop_linear_bwd(const adahop_plan *plan, const void *GY, const void *X, const void *W, int64_t M,
-                                int64_t N, int64_t K, void *dX, void *dW, int out_dtype, void *workspace,
+                                int64_t N, int64_t K, void *dX, void *dW, adahop_out_dtype out_dtype, void *workspace,
                                 size_t ws_bytes, adahop_stream_t stream) {
   if (!GY || !X || !W || (!dX && !dW)) return ADAHOP_ERR_INVALID_ARG;
   if (out_dtype != ADAHOP_OUT_BF16 && out_dtype != ADAHOP_OUT_FP32) return ADAHOP_ERR_INVALID_ARG;
@@ -722,7 +834,7 @@ adahop_status adahop_saved_size(const adahop_plan *plan, int64_t M, int64_t N, i
 }
 
 adahop_status adahop_linear_fwd_save(const adahop_plan *plan, const void *X, const void *W, int64_t M, int64_t N,
-                                     int64_t K, void *Y, int out_dtype, void *saved, size_t saved_bytes,
+                                     int64_t K, void *Y, adahop_out_dtype out_dtype, void *saved, size_t saved_bytes,
                                      void *workspace, size_t ws_bytes, adahop_stream_t stream) {
   if (!X || !W || !Y) return ADAHOP_ERR_INVALID_ARG;
   if (out_dtype != ADAHOP_OUT_BF16 && out_dtype != ADAHOP_OUT_FP32) return ADAHOP_ERR_INVALID_ARG;
@@ -761,7 +873,7 @@ adahop_status adahop_linear_fwd_save(const adahop_plan *plan, const void *X, con
 
 adahop_status adahop_linear_bwd_saved(const adahop_plan *plan, const void *GY, const void *X, const void *W,
                                       const void *saved, size_t saved_bytes, int64_t M, int64_t N, int64_t K,
-                                      void *dX, void *dW, int out_dtype, void *workspace, size_t ws_bytes,
+                                      void *dX, void *dW, adahop_out_dtype out_dtype, void *workspace, size_t ws_bytes,
                                       adahop_stream_t stream) {
   if (!GY || !X || !W || (!dX && !dW)) return ADAHOP_ERR_INVALID_ARG;
   if (out_dtype != ADAHOP_OUT_BF16 && out_dtype != ADAHOP_OUT_FP32) return ADAHOP_ERR_INVALID_ARG;
@@ -831,8 +943,10 @@ adahop_status adahop_probe_copy(const void *src, void *dst, size_t bytes, adahop
   return ADAHOP_OK;
 }
 
+// adahop_foid's workspace: a 256-byte header (the completion counter; zero at the first call,
+// left zero by every call) and then the stage-1 candidates.
 size_t adahop_foid_workspace_size(int64_t lines, int r) {
-  return align256(foid_scratch_bytes(lines, r));
+  return 256 + align256(foid_scratch_bytes(lines, r));
 }
 
 adahop_status adahop_foid(const void *T, int64_t rows, int64_t cols, int axis, int r, int32_t *idx_out,
@@ -842,11 +956,12 @@ adahop_status adahop_foid(const void *T, int64_t rows, int64_t cols, int axis, i
   const int64_t lines = axis == 0 ? rows : cols;
   if (r < 0 || r > kMaxRank || r > lines) return ADAHOP_ERR_SHAPE;
   if ((lines + 2047) / 2048 * static_cast<int64_t>(r) > 8192) return ADAHOP_ERR_SHAPE;
-  if (!aligned(T, 16) || !aligned(workspace, 16)) return ADAHOP_ERR_ALIGN;
+  if (!aligned(T, 16) || !aligned(workspace, 256)) return ADAHOP_ERR_ALIGN;
   if (ws_bytes < adahop_foid_workspace_size(lines, r)) return ADAHOP_ERR_WORKSPACE;
   DeviceInfo di;
   ST_TRY(device_info(&di));
-  CUDA_TRY(launch_foid(static_cast<const uint16_t *>(T), rows, cols, axis, r, idx_out, line_mask_out, workspace,
+  CUDA_TRY(launch_foid(static_cast<const uint16_t *>(T), rows, cols, axis, r, idx_out, line_mask_out,
+                       static_cast<uint8_t *>(workspace) + 256, static_cast<uint32_t *>(workspace),
                        reinterpret_cast<cudaStream_t>(stream)),
            "foid");
   return ADAHOP_OK;
@@ -925,7 +1040,7 @@ adahop_status adahop_gather(const void *T, int64_t rows, int64_t cols, const int
 
 adahop_status adahop_gemm_mxfp4(const uint8_t *a_codes, const uint8_t *a_scales, const uint8_t *b_codes,
                                 const uint8_t *b_scales, int64_t P, int64_t Q, int64_t J, const void *A_o,
-                                const void *B_o, int r, void *C, int out_dtype, void *workspace, size_t ws_bytes,
+                                const void *B_o, int r, void *C, adahop_out_dtype out_dtype, void *workspace, size_t ws_bytes,
                                 adahop_stream_t stream) {
   if (!a_codes || !a_scales || !b_codes || !b_scales || !C || !workspace) return ADAHOP_ERR_INVALID_ARG;
   if (out_dtype != 0 && out_dtype != 1) return ADAHOP_ERR_INVALID_ARG;
@@ -942,7 +1057,7 @@ adahop_status adahop_gemm_mxfp4(const uint8_t *a_codes, const uint8_t *a_scales,
 }
 
 adahop_status adahop_gemm_bf16(const void *A, int a_kmajor, const void *B, int b_kmajor, int64_t P, int64_t Q,
-                               int64_t J, void *C, int out_dtype, int splits, float *c_partial, void *workspace,
+                               int64_t J, void *C, adahop_out_dtype out_dtype, int splits, float *c_partial, void *workspace,
                                size_t ws_bytes, adahop_stream_t stream) {
   if (!A || !B || !workspace || (a_kmajor != 0 && a_kmajor != 1) || (b_kmajor != 0 && b_kmajor != 1))
     return ADAHOP_ERR_INVALID_ARG;
@@ -960,7 +1075,28 @@ adahop_status adahop_gemm_bf16(const void *A, int a_kmajor, const void *B, int b
   return bf16_gemm(cx, A, a_kmajor, B, b_kmajor, P, Q, J, C, out_dtype, splits, c_partial);
 }
 
-adahop_status adahop_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype, const float *partial, int splits,
+adahop_status adahop_gemm_bf16_scatter_add(const void *A, int a_kmajor, const void *B, int b_kmajor, int64_t P,
+                                           int64_t Q, int64_t J, void *C, int64_t c_rows, int64_t c_cols,
+                                           adahop_out_dtype out_dtype, const int32_t *idx, int r, int axis, void *workspace,
+                                           size_t ws_bytes, adahop_stream_t stream) {
+  if (!A || !B || !C || !workspace || (!idx && r > 0) || (a_kmajor != 0 && a_kmajor != 1) ||
+      (b_kmajor != 0 && b_kmajor != 1) || (axis != 0 && axis != 1) || (out_dtype != 0 && out_dtype != 1))
+    return ADAHOP_ERR_INVALID_ARG;
+  if (r < 1 || r > kMaxRank || (axis == 0 ? P != r : Q != r)) return ADAHOP_ERR_SHAPE;
+  if (P <= 0 || Q <= 0 || J <= 0 || J % 64 || c_cols % 8 || c_rows <= 0 || c_cols <= 0) return ADAHOP_ERR_SHAPE;
+  if (axis == 0 && Q != c_cols) return ADAHOP_ERR_SHAPE;
+  if (axis == 1 && P != c_rows) return ADAHOP_ERR_SHAPE;
+  if (a_kmajor ? false : P % 64) return ADAHOP_ERR_SHAPE;
+  if (b_kmajor ? false : Q % 64) return ADAHOP_ERR_SHAPE;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(workspace, 256)) return ADAHOP_ERR_ALIGN;
+  if (ws_bytes < 256) return ADAHOP_ERR_WORKSPACE;
+  DeviceInfo di;
+  ST_TRY(device_info(&di));
+  Ctx cx{reinterpret_cast<cudaStream_t>(stream), static_cast<uint8_t *>(workspace), GemmWs{}, di.num_sms};
+  return bf16_scatter_gemm(cx, A, a_kmajor, B, b_kmajor, P, Q, J, C, c_rows, c_cols, out_dtype, idx, axis);
+}
+
+adahop_status adahop_scatter_add(void *C, int64_t P, int64_t Q, adahop_out_dtype out_dtype, const float *partial, int splits,
                                  const int32_t *idx, int r, int axis, adahop_stream_t stream) {
   if (!C || !partial || (!idx && r > 0) || (axis != 0 && axis != 1) || splits < 1) return ADAHOP_ERR_INVALID_ARG;
   if (out_dtype != 0 && out_dtype != 1) return ADAHOP_ERR_INVALID_ARG;

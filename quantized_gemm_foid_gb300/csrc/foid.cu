@@ -16,9 +16,12 @@
 // run remains, written out as the chunk's r candidates.  A merge level is one pass: output i of
 // the best keys of sorted runs A and B is max(A[a], B[i - a]), where a, the number of A's keys
 // among the i best, comes from a binary search (A[m] belongs to the i best iff A[m] > B[i - m - 1]).
-// Stage 2 (one CTA): each warp holds a run of the best keys in its registers and folds the
-// chunks' runs into it with bitonic merges (shuffles, no shared-memory searches); a tree over the
-// warps leaves the global best r in one warp, which sorts their lines ascending.
+// Stage 2, in the same launch: every stage-1 CTA writes its candidates and counts itself done on
+// a counter; the CTA that finishes last (no CTA waits for another) merges all of them: each warp
+// holds a run of the best keys in its registers and folds the chunks' runs into it with bitonic
+// merges (shuffles, no shared-memory searches); a tree over the warps leaves the global best r in
+// one warp, which sorts their lines ascending.  The last CTA then sets the counter back to zero,
+// so it starts every call at zero.
 #include <mutex>
 
 #include "common.cuh"
@@ -130,17 +133,25 @@ __device__ __forceinline__ uint64_t merge_at(const uint64_t *A, int la, const ui
   return A[lo] > B[b] ? A[lo] : B[b];
 }
 
-template <int AXIS>
-__global__ void __launch_bounds__(kFoidThreads) foid_local_kernel(const uint16_t *__restrict__ T,
-                                                                  int64_t rows, int64_t cols, int r,
-                                                                  int chunk, uint64_t *cand) {
+template <int KPL>
+__device__ void foid_finish(uint32_t *counter, uint64_t *sk, const uint64_t *cand, int runs, int r, int64_t lines,
+                            int32_t *idx_out, uint32_t *mask_out);
+
+// Stage 1 for column probes (strided loads): each warp scores 32 columns at a time and sorts them
+// in registers, then merge levels in shared memory keep the best r of each merged pair until one
+// run remains, written out as the chunk's r candidates; the last CTA to finish merges all chunks.
+template <int KPL>
+__global__ void __launch_bounds__(kFoidThreads) foid_local_cols_kernel(const uint16_t *__restrict__ T,
+                                                                       int64_t rows, int64_t cols, int r,
+                                                                       int chunk, uint64_t *cand, uint32_t *counter,
+                                                                       int32_t *idx_out, uint32_t *mask_out) {
   __shared__ uint64_t keys[2][kFoidMaxChunk];
-  const int64_t lines = AXIS == 0 ? rows : cols;
+  const int64_t lines = cols;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * chunk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   for (int r0 = 32 * warp; r0 < chunk; r0 += 32 * nwarps) {
     const int64_t line = base + r0 + lane;
-    const uint64_t key = line < lines ? foid_key<AXIS>(T, cols, line) : 0ull;
+    const uint64_t key = line < lines ? foid_key<1>(T, cols, line) : 0ull;
     keys[0][r0 + lane] = warp_sort_desc(key);
   }
   __syncthreads();
@@ -161,6 +172,8 @@ __global__ void __launch_bounds__(kFoidThreads) foid_local_kernel(const uint16_t
   }
   for (int i = tid; i < r; i += blockDim.x)
     cand[static_cast<int64_t>(blockIdx.x) * r + i] = i < len ? keys[src][i] : 0ull;
+  __syncthreads();                             // keys[] is reused by the merge below
+  foid_finish<KPL>(counter, &keys[0][0], cand, static_cast<int>(gridDim.x), r, lines, idx_out, mask_out);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -171,8 +184,6 @@ __global__ void __launch_bounds__(kFoidThreads) foid_local_kernel(const uint16_t
 // strides R/2, ..., 1 sort it -- strides of 32 and more between a lane's registers, smaller ones
 // across lanes by shuffles.  No shared-memory searches, no bank conflicts.
 // ---------------------------------------------------------------------------------------------
-constexpr int kMergeThreads = 512;            // 16 warps
-constexpr int kMergeWarps = kMergeThreads / 32;
 
 __device__ __forceinline__ uint64_t kmax(uint64_t a, uint64_t b) { return a > b ? a : b; }
 __device__ __forceinline__ uint64_t kmin(uint64_t a, uint64_t b) { return a < b ? a : b; }
@@ -248,7 +259,8 @@ __device__ __forceinline__ void warp_sort_asc(uint32_t (&v)[KPL], int lane) {
 template <int KPL>
 __global__ void __launch_bounds__(kFoidThreads, 1) foid_local_rows_kernel(const uint16_t *__restrict__ T,
                                                                        int64_t rows, int64_t cols, int r,
-                                                                       int chunk, uint64_t *cand) {
+                                                                       int chunk, uint64_t *cand, uint32_t *counter,
+                                                                       int32_t *idx_out, uint32_t *mask_out) {
   __shared__ uint64_t sk[kFoidThreads / 32][32 * KPL];
   const int64_t base = static_cast<int64_t>(blockIdx.x) * chunk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -283,18 +295,21 @@ __global__ void __launch_bounds__(kFoidThreads, 1) foid_local_rows_kernel(const 
       if (e < r) cand[static_cast<int64_t>(blockIdx.x) * r + e] = top[s];
     }
   }
+  __syncthreads();                             // sk[] is reused by the merge below
+  foid_finish<KPL>(counter, &sk[0][0], cand, static_cast<int>(gridDim.x), r, rows, idx_out, mask_out);
 }
 
-// Stage 2: runs x r candidates (each run sorted descending, r keys).  Every warp folds its share
-// of the runs into one run of the R largest, a tree over the warps through shared memory leaves
-// the R largest in warp 0, whose first r are the selection; warp 0 then sorts their lines
-// ascending, writes them and sets their bits in the line bitmap (cleared first by all threads).
+// Stage 2: runs x r candidates (each run sorted descending, r keys) at `cand`, merged by the
+// calling CTA (nwarps = blockDim / 32, a power of two; sk holds nwarps x 32 KPL keys).  Every warp
+// folds its share of the runs into one run of the R largest, a tree over the warps through shared
+// memory leaves the R largest in warp 0, whose first r are the selection; warp 0 then sorts their
+// lines ascending, writes them and sets their bits in the line bitmap (cleared first by all
+// threads).  The candidates are read from L2 (written by other CTAs of the same launch).
 template <int KPL>
-__global__ void __launch_bounds__(kMergeThreads) foid_merge_kernel(const uint64_t *cand, int runs, int r,
-                                                                   int64_t lines, int32_t *idx_out,
-                                                                   uint32_t *mask_out) {
-  __shared__ uint64_t sk[kMergeWarps][32 * KPL];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ void foid_merge_cta(uint64_t *sk_flat, const uint64_t *cand, int runs, int r, int64_t lines,
+                               int32_t *idx_out, uint32_t *mask_out) {
+  uint64_t (*sk)[32 * KPL] = reinterpret_cast<uint64_t (*)[32 * KPL]>(sk_flat);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int64_t words = (lines + 31) >> 5;
   if (mask_out) {
     for (int64_t w = tid; w < words; w += blockDim.x) mask_out[w] = 0u;
@@ -304,16 +319,15 @@ __global__ void __launch_bounds__(kMergeThreads) foid_merge_kernel(const uint64_
 #pragma unroll
   for (int s = 0; s < KPL; ++s) top[s] = 0ull;
   // four runs' loads in flight per warp, then their merges
-  for (int run0 = warp; run0 < runs; run0 += 4 * kMergeWarps) {
+  for (int run0 = warp; run0 < runs; run0 += 4 * nwarps) {
     uint64_t b[4][KPL];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int run = run0 + u * kMergeWarps;
-      if (run < runs) {
-        run_load<KPL>(b[u], cand + static_cast<int64_t>(run) * r, r, lane);
-      } else {
+      const int run = run0 + u * nwarps;
 #pragma unroll
-        for (int s = 0; s < KPL; ++s) b[u][s] = 0ull;
+      for (int s = 0; s < KPL; ++s) {
+        const int e = 32 * s + lane;
+        b[u][s] = (run < runs && e < r) ? __ldcg(cand + static_cast<int64_t>(run) * r + e) : 0ull;
       }
     }
 #pragma unroll
@@ -322,8 +336,7 @@ __global__ void __launch_bounds__(kMergeThreads) foid_merge_kernel(const uint64_
 #pragma unroll
   for (int s = 0; s < KPL; ++s) sk[warp][32 * s + lane] = top[s];
   __syncthreads();                            // also orders the bitmap clearing before the bits below
-#pragma unroll
-  for (int half = kMergeWarps / 2; half >= 1; half >>= 1) {
+  for (int half = nwarps / 2; half >= 1; half >>= 1) {
     if (warp < half) {
       uint64_t b[KPL];
       run_load<KPL>(b, sk[warp + half], 32 * KPL, lane);
@@ -352,6 +365,29 @@ __global__ void __launch_bounds__(kMergeThreads) foid_merge_kernel(const uint64_
   }
 }
 
+// End of every stage-1 CTA: publish the candidates, count this CTA done; the CTA whose count
+// completes the grid merges everything and resets the counter.  No CTA waits for another.
+template <int KPL>
+__device__ void foid_finish(uint32_t *counter, uint64_t *sk, const uint64_t *cand, int runs, int r, int64_t lines,
+                            int32_t *idx_out, uint32_t *mask_out) {
+  __shared__ int is_last;
+  __threadfence();                           // this thread's candidates are visible before the count
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(counter, 1u) == gridDim.x - 1u;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();                           // the other CTAs' candidates are read after their counts
+  foid_merge_cta<KPL>(sk, cand, runs, r, lines, idx_out, mask_out);
+  if (threadIdx.x == 0) *counter = 0u;       // every call starts at zero
+}
+
+// r = 0: only the line bitmap is written (cleared).
+__global__ void foid_clear_kernel(int64_t lines, uint32_t *mask_out) {
+  const int64_t words = (lines + 31) >> 5;
+  if (mask_out)
+    for (int64_t w = threadIdx.x; w < words; w += blockDim.x) mask_out[w] = 0u;
+}
+
 }  // namespace
 
 size_t foid_scratch_bytes(int64_t lines, int r) {
@@ -361,36 +397,37 @@ size_t foid_scratch_bytes(int64_t lines, int r) {
 }
 
 cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
-                        int32_t *idx_out, uint32_t *mask_out, void *scratch, cudaStream_t s) {
+                        int32_t *idx_out, uint32_t *mask_out, void *scratch, uint32_t *counter, cudaStream_t s) {
   const int64_t lines = axis == 0 ? rows : cols;
   if (r < 0 || r > 256) return cudaErrorInvalidValue;
+  if (r == 0) {
+    foid_clear_kernel<<<1, 256, 0, s>>>(lines, mask_out);
+    return cudaGetLastError();
+  }
   const int chunk = foid_chunk(lines, r);
   const int64_t chunks = (lines + chunk - 1) / chunk;
   if (chunks * r > kFoidMergeMaxKeys) return cudaErrorInvalidValue;
   uint64_t *cand = static_cast<uint64_t *>(scratch);
-  if (r > 0) {
-    const int threads = chunk < kFoidThreads ? chunk : kFoidThreads;
-    const unsigned grid = static_cast<unsigned>(chunks);
-    if (axis == 1)
-      foid_local_kernel<1><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
-    else if (r <= 32)
-      foid_local_rows_kernel<1><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
-    else if (r <= 64)
-      foid_local_rows_kernel<2><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
-    else if (r <= 128)
-      foid_local_rows_kernel<4><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
-    else
-      foid_local_rows_kernel<8><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand);
-  }
-  const int runs = r > 0 ? static_cast<int>(chunks) : 0;
+  const int threads = chunk < kFoidThreads ? chunk : kFoidThreads;
+  const unsigned grid = static_cast<unsigned>(chunks);
+#define ADAHOP_FOID_LAUNCH(KPL)                                                                             \
+  do {                                                                                                      \
+    if (axis == 1)                                                                                          \
+      foid_local_cols_kernel<KPL><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand, counter, idx_out, \
+                                                           mask_out);                                       \
+    else                                                                                                    \
+      foid_local_rows_kernel<KPL><<<grid, threads, 0, s>>>(T, rows, cols, r, chunk, cand, counter, idx_out, \
+                                                           mask_out);                                       \
+  } while (0)
   if (r <= 32)
-    foid_merge_kernel<1><<<1, kMergeThreads, 0, s>>>(cand, runs, r, lines, idx_out, mask_out);
+    ADAHOP_FOID_LAUNCH(1);
   else if (r <= 64)
-    foid_merge_kernel<2><<<1, kMergeThreads, 0, s>>>(cand, runs, r, lines, idx_out, mask_out);
+    ADAHOP_FOID_LAUNCH(2);
   else if (r <= 128)
-    foid_merge_kernel<4><<<1, kMergeThreads, 0, s>>>(cand, runs, r, lines, idx_out, mask_out);
+    ADAHOP_FOID_LAUNCH(4);
   else
-    foid_merge_kernel<8><<<1, kMergeThreads, 0, s>>>(cand, runs, r, lines, idx_out, mask_out);
+    ADAHOP_FOID_LAUNCH(8);
+#undef ADAHOP_FOID_LAUNCH
   return cudaGetLastError();
 }
 
@@ -399,36 +436,83 @@ cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis,
 //
 // Some callers only own their inputs and outputs: a plug-in or callback running inside another
 // runtime that manages all device memory itself, or a code path that must not call cudaMalloc
-// (it can synchronise the device and fail at run time).  For them the candidate keys of stage 1
-// live in the fixed array below instead of a workspace.  It holds kFoidStaticKeys = 8192 keys
-// (64 KB), the same ceiling the merge stage already has, on every GPU that loads the library,
-// for the life of the process.  Stage 1 writes every slot that stage 2 reads, so nothing in it
-// has to start at zero; it keeps whatever the last call wrote.  All calls share it: two calls
-// whose kernels overlap on the GPU (e.g. on two streams) race on it.
+// (it can synchronise the device and fail at run time).  For them FOID's scratch lives in the
+// fixed array below instead of a workspace: a 256-byte header holding the completion counter of
+// the single launch, then kFoidStaticKeys = 8192 candidate keys (the ceiling the merge already
+// has); 64.25 KB on every GPU that loads the library, for the life of the process.  Device
+// globals start at zero and every call leaves the counter at zero again; stage 1 writes every
+// candidate slot the merge reads, so nothing else has to start at zero, and the array keeps
+// whatever the last call wrote.  All calls share it: two calls whose kernels overlap on the GPU
+// (e.g. on two streams) race on it.
 // ---------------------------------------------------------------------------------------------
 constexpr int kFoidStaticKeys = kFoidMergeMaxKeys;
-static __device__ __align__(256) uint64_t g_foid_static_keys[kFoidStaticKeys];
+constexpr int kFoidStaticHeader = 32;            // uint64 words (256 bytes) before the keys
+static __device__ __align__(256) uint64_t g_foid_static_keys[kFoidStaticHeader + kFoidStaticKeys];
 
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_static_keys_mutex;
-void *g_static_keys_addr[kMaxDevices] = {};   // device address of the array, per device
+// Per device: the array's device address and the id of the context it was looked up in.  A
+// device reset (cudaDeviceReset) destroys the context and with it the module holding the array;
+// the next context gets a new id, so the address is looked up again rather than reused.
+struct StaticKeys {
+  void *addr = nullptr;
+  unsigned long long ctx_id = 0;
+};
+StaticKeys g_static_keys[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// Unique id of the calling thread's current context (driver entry points fetched once).
+cudaError_t current_context_id(unsigned long long *id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+  if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
 
 // The array's name is only a host-side stand-in; its device address comes from the runtime,
-// looked up once per device with that device current.
+// looked up with the device current, once per device and context.
 cudaError_t static_keys_address(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long ctx_id = 0;
+  // With no context current yet (nothing has touched this device on this thread), the lookup
+  // below creates the device's primary context; its id is read after it.
+  const bool have_ctx = current_context_id(&ctx_id) == cudaSuccess;
   std::lock_guard<std::mutex> lock(g_static_keys_mutex);
-  if (!g_static_keys_addr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_foid_static_keys);
-    if (e != cudaSuccess) return e;
-    g_static_keys_addr[dev] = p;
+  StaticKeys &k = g_static_keys[dev];
+  if (have_ctx && k.addr && k.ctx_id == ctx_id) {
+    *out = k.addr;
+    return cudaSuccess;
   }
-  *out = g_static_keys_addr[dev];
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_foid_static_keys);
+  if (e != cudaSuccess) return e;
+  if (!have_ctx) {
+    e = current_context_id(&ctx_id);
+    if (e != cudaSuccess) return e;
+  }
+  k.addr = p;
+  k.ctx_id = ctx_id;
+  *out = p;
   return cudaSuccess;
 }
 }  // namespace
@@ -437,10 +521,12 @@ int64_t foid_static_capacity() { return kFoidStaticKeys; }
 
 cudaError_t launch_foid_noalloc(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
                                 int32_t *idx_out, uint32_t *mask_out, cudaStream_t s) {
-  void *keys = nullptr;
-  cudaError_t e = static_keys_address(&keys);
+  void *base = nullptr;
+  cudaError_t e = static_keys_address(&base);
   if (e != cudaSuccess) return e;
-  return launch_foid(T, rows, cols, axis, r, idx_out, mask_out, keys, s);
+  uint64_t *words = static_cast<uint64_t *>(base);
+  return launch_foid(T, rows, cols, axis, r, idx_out, mask_out, words + kFoidStaticHeader,
+                     reinterpret_cast<uint32_t *>(words), s);
 }
 
 }  // namespace adahop

@@ -51,9 +51,14 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;              // scale factors live above the accumulator
 
 // ------------------------------------------------------------------ kind 0: MXFP4 on CTA pairs
-struct PairCfg {
+// STAGES: main-loop pipeline depth; EPI_BUFS: 1 KB TMA-store staging buffers per epilogue warp.
+// Long inner dimensions keep six stages and one buffer; short ones (J <= 2048, a tile's main loop
+// is a handful of stages) are bound by the stream of output stores, so they trade stages for
+// stores in flight.
+template <int STAGES, int EPI_BUFS>
+struct PairCfgT {
   static constexpr int kBM = 256;                  // rows of C per pair (128 per CTA)
-  static constexpr int kStages = 6;
+  static constexpr int kStages = STAGES;
   static constexpr int kBK = 256;                  // J elements per main-loop stage
   static constexpr uint32_t kABytes = 128 * 128;   // this CTA's 128 rows x 128 bytes of codes
   static constexpr uint32_t kBBytes = 128 * 128;   // this CTA's 128 of the 256 B rows
@@ -65,14 +70,18 @@ struct PairCfg {
   static constexpr uint32_t kTxMain = 2 * kStageBytes;
   static constexpr uint32_t kTxTail = 2 * (kABytes + kBBytes);
   // epilogue staging: per epilogue warp kEpiBufs buffers of 32 rows x 32 bytes (TMA store boxes)
-  static constexpr int kEpiBufs = 1;
+  static constexpr int kEpiBufs = EPI_BUFS;
   static constexpr uint32_t kEpiBufBytes = 1024;
   static constexpr uint32_t kEpiOffset = kStages * kStageBytes;
   static constexpr uint32_t kSmemBytes = kEpiOffset + kEpiWarps * kEpiBufs * kEpiBufBytes;
+  static_assert(kEpiOffset % 1024 == 0, "epilogue buffers need the swizzle alignment");
+  static_assert(kStageBytes % 1024 == 0, "stage layout");
+  static_assert(kSfTmemBase + kStages * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory per CTA");
 };
-static_assert(PairCfg::kEpiOffset % 1024 == 0, "epilogue buffers need the swizzle alignment");
-static_assert(PairCfg::kStageBytes % 1024 == 0, "stage layout");
-static_assert(kSfTmemBase + PairCfg::kStages * PairCfg::kSfCols <= kTmemCols, "TMEM budget");
+using PairCfg = PairCfgT<6, 1>;          // J > 2048
+using PairCfgShortJ = PairCfgT<4, 8>;    // J <= 2048
+constexpr int64_t kShortJ = 2048;
 
 // ------------------------------------------------------------------ kind 1: BF16 on single CTAs
 struct Bf16Cfg {
@@ -171,9 +180,9 @@ __device__ __forceinline__ void store_row32(const GemmArgs &g, bool to_partial, 
 // =============================================================================================
 // kind 0: MXFP4 (+ BF16 outlier tail), CTA pairs
 // =============================================================================================
+template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
-  using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   __shared__ SmemCtl<C::kStages> ctl;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // same offset in both CTAs
@@ -661,6 +670,245 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// =============================================================================================
+// kind 2: BF16 outlier GEMM of outer OE with the scatter-add fused (appendix, Fused Scatter-Add:
+// the outlier product is added in place, with no intermediate result written out).  The product
+// has only r rows (or columns), so its J range is split over the S CTAs of a cluster (S = 1, 2, 4
+// or 8; one (tile, J range) per CTA).  Each CTA leaves its float32 partial tile in its own shared
+// memory; after a cluster barrier CTA k sums rows [k 128/S, (k+1) 128/S) of the tile over the S
+// partials in rank order (through distributed shared memory), adds the sum to C's current value
+// in float32 and rounds once to C's type: C[idx[i], q] += O[i, q] (axis 0) or C[p, idx[i]] +=
+// O[p, i] (axis 1).  A second cluster barrier keeps every partial alive until all are read.
+// =============================================================================================
+constexpr uint32_t kPartialRowBytes = 256 * 4 + 16;   // padded: conflict-free 16-byte row writes
+
+__device__ __forceinline__ void scatter_add4(const GemmArgs &g, int64_t row, int64_t col, const float4 &o) {
+  const float add[4] = {o.x, o.y, o.z, o.w};
+  if (g.scatter_axis == 0) {
+    const int64_t dst = g.scatter_idx[row];
+    if (dst < 0 || dst >= g.c_rows || col + 4 > g.c_cols) return;   // never write outside C
+    if (g.out_dtype == 1) {
+      float4 *p = reinterpret_cast<float4 *>(static_cast<float *>(g.C) + dst * g.c_cols + col);
+      float4 c = *p;
+      c.x += add[0]; c.y += add[1]; c.z += add[2]; c.w += add[3];
+      *p = c;
+    } else {
+      uint2 *p = reinterpret_cast<uint2 *>(static_cast<uint16_t *>(g.C) + dst * g.c_cols + col);
+      const uint2 c = *p;
+      const uint32_t w0 = pack_bf16x2_rn(bf16_bits_to_f32(c.x & 0xFFFFu) + add[0], bf16_bits_to_f32(c.x >> 16) + add[1]);
+      const uint32_t w1 = pack_bf16x2_rn(bf16_bits_to_f32(c.y & 0xFFFFu) + add[2], bf16_bits_to_f32(c.y >> 16) + add[3]);
+      *p = make_uint2(w0, w1);
+    }
+  } else {
+    if (row >= g.c_rows) return;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (col + e >= g.Q) break;
+      const int64_t dst = g.scatter_idx[col + e];
+      if (dst < 0 || dst >= g.c_cols) continue;
+      if (g.out_dtype == 1) {
+        float *p = static_cast<float *>(g.C) + row * g.c_cols + dst;
+        *p = *p + add[e];
+      } else {
+        uint16_t *p = static_cast<uint16_t *>(g.C) + row * g.c_cols + dst;
+        *p = static_cast<uint16_t>(f32_to_bf16_bits(bf16_bits_to_f32(*p) + add[e]));
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_scatter_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
+  using C = Bf16Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ SmemCtl<C::kStages> ctl;
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // swizzle atoms need alignment
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t split = cluster_ctarank();
+  const uint32_t nsplit = cluster_nctarank();
+  const int64_t tile = blockIdx.x / nsplit;
+  const int num_k = static_cast<int>((g.J + C::kBK - 1) / C::kBK);
+  const int64_t tiles_n = (g.Q + BN - 1) / BN;
+  const int64_t m0 = (tile / tiles_n) * C::kBM, n0 = (tile % tiles_n) * BN;
+  const int per = (num_k + static_cast<int>(nsplit) - 1) / static_cast<int>(nsplit);
+  const int k_begin = min(num_k, static_cast<int>(split) * per);
+  const int k_end = min(num_k, k_begin + per);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&ctl.full[s]), 1);
+      mbar_init(smem_u32(&ctl.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&ctl.acc_full), 1);
+    mbar_init(smem_u32(&ctl.drain), 1);
+    ctl.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl.tmem_base), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int *abort_flag = &ctl.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      prefetch_tensormap(&maps.a);
+      prefetch_tensormap(&maps.b);
+    }
+    __syncwarp();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int ks = k_begin; ks < k_end; ++ks) {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, 32))) {
+        ok = false;
+        break;
+      }
+      const uint32_t sA = smem_base + stage * C::kStageBytes;
+      const uint32_t sB = sA + C::kABytes;
+      const uint32_t full = smem_u32(&ctl.full[stage]);
+      if (elect_one()) {
+        mbar_arrive_expect_tx(full, C::kABytes + C::kBBytes);
+        const int32_t k0 = ks * 64;
+        if (g.a_mn_major) {
+          tma_load_2d(sA, &maps.a, full, static_cast<int32_t>(m0), k0);
+          tma_load_2d(sA + 8192, &maps.a, full, static_cast<int32_t>(m0 + 64), k0);
+        } else {
+          tma_load_2d(sA, &maps.a, full, k0, static_cast<int32_t>(m0));
+        }
+        if (g.b_mn_major) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * 8192, &maps.b, full, static_cast<int32_t>(n0 + 64 * c), k0);
+        } else {
+          tma_load_2d(sB, &maps.b, full, k0, static_cast<int32_t>(n0));
+        }
+      }
+      __syncwarp();
+      if (++stage == C::kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report_status(g.status, kStatusTimeout);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    const uint32_t idesc = make_idesc_bf16(C::kBM, BN, g.a_mn_major != 0, g.b_mn_major != 0);
+    for (int ks = k_begin; ks < k_end; ++ks) {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sA = smem_base + stage * C::kStageBytes;
+      const uint32_t sB = sA + C::kABytes;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t adesc = g.a_mn_major ? make_smem_desc(sA + 2048 * kk, 8192, 1024, kLayoutSw128)
+                                              : make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
+          const uint64_t bdesc = g.b_mn_major ? make_smem_desc(sB + 2048 * kk, 8192, 1024, kLayoutSw128)
+                                              : make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
+          mma_bf16(tmem, adesc, bdesc, idesc, (ks > k_begin || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&ctl.empty[stage]));
+      }
+      __syncwarp();
+      if (++stage == C::kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (ok && elect_one()) tc_commit(smem_u32(&ctl.acc_full));   // the partial is in tensor memory
+    __syncwarp();
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report_status(g.status, kStatusTimeout);
+    }
+    if (elect_one()) tc_commit(smem_u32(&ctl.drain));
+    __syncwarp();
+    if (!mbar_wait(smem_u32(&ctl.drain), 0, nullptr) && lane == 0) report_status(g.status, kStatusTimeout);
+  } else {
+    // ------------------------------------------------------------------ partial -> shared memory
+    // The pipeline is drained once the accumulator is ready (every MMA, hence every operand load,
+    // has completed), so the stage buffers hold the partial tile: 128 rows of 256 floats.
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    bool ready = true;
+    if (k_end > k_begin) {
+      if (lane == 0) ready = mbar_wait(smem_u32(&ctl.acc_full), 0, abort_flag, 128);
+      ready = __shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0) != 0;
+    }
+    if (!ready) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        report_status(g.status, kStatusTimeout);
+      }
+    } else {
+      tc_fence_after();
+      const uint32_t row_addr = smem_base + static_cast<uint32_t>(32 * quad + lane) * kPartialRowBytes;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t v[32];
+        if (k_end > k_begin) {
+          tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + 128u * half + 32u * j, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;             // an empty J range adds zeros
+        }
+        const uint32_t a = row_addr + (128u * half + 32u * j) * 4u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) st_shared_v4(a + 16u * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    }
+  }
+
+  // every partial of the cluster is in shared memory (or its CTA gave up)
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp >= 2) {
+    bool any_abort = false;
+    for (uint32_t k = 0; k < nsplit; ++k) any_abort |= ld_cluster_u32(cluster_map(smem_u32(&ctl.abort_flag), k)) != 0;
+    if (!any_abort) {
+      const int te = threadIdx.x - 64;                        // 256 reducing threads
+      const int rows_per = C::kBM / static_cast<int>(nsplit);
+      const int items = rows_per * (BN / 4);
+      for (int it = te; it < items; it += kEpiWarps * 32) {
+        const int rr = static_cast<int>(split) * rows_per + it / (BN / 4);
+        const int c4 = it % (BN / 4);
+        const int64_t row = m0 + rr, col = n0 + 4 * c4;
+        if (row >= g.P || col >= g.Q) continue;
+        const uint32_t off = smem_base + static_cast<uint32_t>(rr) * kPartialRowBytes + 16u * c4;
+        float4 acc = ld_cluster_v4(cluster_map(off, 0));
+        for (uint32_t k = 1; k < nsplit; ++k) {
+          const float4 o = ld_cluster_v4(cluster_map(off, k));
+          acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+        }
+        scatter_add4(g, row, col, acc);
+      }
+    }
+  }
+  cluster_sync_all();                                 // no CTA leaves while its partial may be read
+  if (*abort_flag) {
+    if (threadIdx.x == 0) settle_inflight_loads();
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
 // attr must hold two entries: the cluster shape and programmatic dependent launch (pdl_enter).
 cudaLaunchConfig_t pair_launch_config(cudaLaunchAttribute *attr, unsigned grid, size_t smem, cudaStream_t s) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -679,7 +927,9 @@ cudaLaunchConfig_t pair_launch_config(cudaLaunchAttribute *attr, unsigned grid, 
   return cfg;
 }
 
-// Co-resident CTA pairs of the MXFP4 kernel on the current device (its persistent grid), cached.
+// Co-resident CTA pairs of the MXFP4 kernel (configuration C) on the current device (its
+// persistent grid), cached per device.
+template <class C>
 int pair_capacity(int num_sms) {
   constexpr int kMaxDevices = 64;
   static int cached[kMaxDevices] = {};
@@ -687,9 +937,10 @@ int pair_capacity(int num_sms) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return num_sms / 2;
   if (cached[dev] > 0) return cached[dev];
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = pair_launch_config(attr, static_cast<unsigned>(num_sms & ~1), gemm_smem_bytes(0), 0);
+  const cudaLaunchConfig_t cfg =
+      pair_launch_config(attr, static_cast<unsigned>(num_sms & ~1), C::kSmemBytes + 1024, 0);
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf4_pair_kernel, &cfg) != cudaSuccess || clusters <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf4_pair_kernel<C>, &cfg) != cudaSuccess || clusters <= 0) {
     (void)cudaGetLastError();
     clusters = num_sms / 2;
   }
@@ -697,19 +948,25 @@ int pair_capacity(int num_sms) {
   return clusters;
 }
 
-cudaError_t launch_mxf4(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
-  const size_t smem = gemm_smem_bytes(0);
-  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <class C>
+cudaError_t launch_mxf4_cfg(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
+  const size_t smem = C::kSmemBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int64_t tiles = ((g.P + PairCfg::kBM - 1) / PairCfg::kBM) * ((g.Q + BN - 1) / BN);
-  const int64_t cap = pair_capacity(num_sms);
+  const int64_t tiles = ((g.P + C::kBM - 1) / C::kBM) * ((g.Q + BN - 1) / BN);
+  const int64_t cap = pair_capacity<C>(num_sms);
   const unsigned pairs = static_cast<unsigned>(tiles < cap ? tiles : cap);
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_launch_config(attr, 2 * pairs, smem, s);
-  e = cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, maps, g);
+  e = cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<C>, maps, g);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+cudaError_t launch_mxf4(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
+  return g.J <= kShortJ ? launch_mxf4_cfg<PairCfgShortJ>(g, maps, num_sms, s)
+                        : launch_mxf4_cfg<PairCfg>(g, maps, num_sms, s);
 }
 
 cudaError_t launch_bf16(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
@@ -724,17 +981,55 @@ cudaError_t launch_bf16(const GemmArgs &g, const GemmMaps &maps, int num_sms, cu
   return cudaGetLastError();
 }
 
+int scatter_splits(int64_t P, int64_t Q, int64_t J, int num_sms) {
+  const int64_t tiles = ((P + Bf16Cfg::kBM - 1) / Bf16Cfg::kBM) * ((Q + BN - 1) / BN);
+  const int64_t k_stages = (J + Bf16Cfg::kBK - 1) / Bf16Cfg::kBK;
+  int s = 1;
+  while (s < 8 && tiles * (2 * s) <= num_sms && k_stages >= 4 * (2 * s)) s *= 2;
+  return s;
+}
+
+cudaError_t launch_bf16_scatter(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
+  const size_t smem = gemm_smem_bytes(1);
+  static_assert(Bf16Cfg::kBM * kPartialRowBytes <= Bf16Cfg::kStages * Bf16Cfg::kStageBytes,
+                "the partial tile must fit the stage buffers");
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int splits = scatter_splits(g.P, g.Q, g.J, num_sms);
+  const int64_t tiles = ((g.P + Bf16Cfg::kBM - 1) / Bf16Cfg::kBM) * ((g.Q + BN - 1) / BN);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * splits), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_bf16_scatter_kernel, maps, g);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
+int scatter_gemm_splits(int64_t P, int64_t Q, int64_t J, int num_sms) { return scatter_splits(P, Q, J, num_sms); }
+
 size_t gemm_smem_bytes(int kind) {
-  return kind == 0 ? PairCfg::kSmemBytes + 1024
+  return kind == 0 ? (PairCfg::kSmemBytes > PairCfgShortJ::kSmemBytes ? PairCfg::kSmemBytes : PairCfgShortJ::kSmemBytes) + 1024
                    : Bf16Cfg::kStages * Bf16Cfg::kStageBytes + 1024;
 }
 
 int gemm_tail_cols_per_stage() { return 64; }
 
 cudaError_t launch_gemm(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
-  return g.kind == 0 ? launch_mxf4(g, maps, num_sms, s) : launch_bf16(g, maps, num_sms, s);
+  if (g.kind == 0) return launch_mxf4(g, maps, num_sms, s);
+  if (g.kind == 2) return launch_bf16_scatter(g, maps, num_sms, s);
+  return launch_bf16(g, maps, num_sms, s);
 }
 
 }  // namespace adahop

@@ -30,10 +30,12 @@ cudaError_t launch_quant(const QuantArgs &a, int inner_axis, int num_sms, cudaSt
 // codes_cols / scales_cols the J = rows orientation (lines = cols); same masks and Hadamard flag.
 cudaError_t launch_quant_dual(const QuantArgs &a, uint8_t *codes_cols, uint8_t *scales_cols, cudaStream_t s);
 
-// FOID: stage 1 (per-chunk top-r of 256..2048 lines) + stage 2 (merge, ascending indices, bitmap).
+// FOID in one launch: stage 1 (per-chunk top-r of 256..2048 lines), then the last CTA to finish
+// merges (ascending indices, bitmap).  scratch: foid_scratch_bytes() of candidates; counter: one
+// uint32 that must be zero when the launch starts (the launch leaves it zero).
 size_t foid_scratch_bytes(int64_t lines, int r);
 cudaError_t launch_foid(const uint16_t *T, int64_t rows, int64_t cols, int axis, int r,
-                        int32_t *idx_out, uint32_t *mask_out, void *scratch, cudaStream_t s);
+                        int32_t *idx_out, uint32_t *mask_out, void *scratch, uint32_t *counter, cudaStream_t s);
 
 // FOID with its candidate keys in a fixed device array instead of caller scratch (see foid.cu).
 int64_t foid_static_capacity();
@@ -42,6 +44,18 @@ cudaError_t launch_foid_noalloc(const uint16_t *T, int64_t rows, int64_t cols, i
 
 cudaError_t launch_gather(const uint16_t *T, int64_t rows, int64_t cols, const int32_t *idx, int r,
                           int mode, uint16_t *out, cudaStream_t s);
+// Several gathers (modes of launch_gather) in one launch, each on its own range of CTAs.
+struct GatherJob {
+  const uint16_t *T;
+  int64_t rows, cols;
+  const int32_t *idx;
+  int r;
+  int mode;
+  uint16_t *out;
+  int r_out;   // modes 1 / 2: values per output line (>= r; entries r .. r_out - 1 are +0); 0 = r
+};
+constexpr int kMaxGatherJobs = 4;
+cudaError_t launch_gathers(const GatherJob *jobs, int count, cudaStream_t s);
 
 cudaError_t launch_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype, const float *partial,
                                int splits, const int32_t *idx, int r, int axis, cudaStream_t s);
@@ -68,6 +82,12 @@ struct GemmArgs {
   int splits;                 // BF16: split-K count (>= 1)
   float *c_partial;           // non-null: fp32 partials (splits x P x Q) are written here, not C
   uint32_t *status;
+  // kind 2 (BF16 outlier GEMM with the scatter-add fused): the product O (P x Q) is added into the
+  // output C (c_rows x c_cols, out_dtype): scatter_axis 0: C[idx[i], q] += O[i, q] (P = r);
+  // scatter_axis 1: C[p, idx[i]] += O[p, i] (Q = r).  `splits` CTAs of one cluster share a tile.
+  const int32_t *scatter_idx;
+  int scatter_axis;
+  int64_t c_rows, c_cols;
 };
 // MXFP4: a / b are the E2M1 codes (128-byte rows, 128 rows per box), sfa / sfb the tensor-core
 // scale atoms viewed as rows of 128 uint32 (one 512-byte atom per row, two atoms per box), ao / bo
@@ -77,6 +97,8 @@ struct GemmMaps {
   CUtensorMap a, b, ao, bo, sfa, sfb, c;
 };
 cudaError_t launch_gemm(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s);
+// Cluster size (split-K count) the fused outlier GEMM uses for a P x Q x J product.
+int scatter_gemm_splits(int64_t P, int64_t Q, int64_t J, int num_sms);
 size_t gemm_smem_bytes(int kind);
 int gemm_tail_cols_per_stage();
 

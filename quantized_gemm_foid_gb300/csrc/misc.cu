@@ -14,62 +14,64 @@ namespace adahop {
 namespace {
 
 // ------------------------------------------------------------------------------- gathers
+// Each mode is a device function over a virtual grid (block vb of vg, 256 threads) so that one
+// launch can run several gathers side by side (gather_multi_kernel); `tile` is the caller's
+// shared memory (256 x 72 uint16 at most).
+constexpr int kGatherThreads = 256;
+constexpr int kGatherTileElems = 256 * 72;
+
 // mode 0: out[i, :] = T[idx[i], :]   (r x cols), 16-byte copies
-__global__ void gather_rows_kernel(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
-                                   const int32_t *__restrict__ idx, int r, uint16_t *out) {
+__device__ void gather_rows(const uint16_t *__restrict__ T, int64_t rows, int64_t cols, const int32_t *__restrict__ idx,
+                            int r, uint16_t *out, int64_t vb, int64_t vg) {
   const int64_t vec = cols >> 3;
   const int64_t total = static_cast<int64_t>(r) * vec;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
-       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  for (int64_t t = vb * kGatherThreads + threadIdx.x; t < total; t += vg * kGatherThreads) {
     const int64_t i = t / vec, v = t - i * vec;
     const int64_t src = idx[i];
     if (src < 0 || src >= rows) continue;        // indices come from FOID; never read outside T
-    reinterpret_cast<uint4 *>(out + i * cols)[v] =
-        __ldg(reinterpret_cast<const uint4 *>(T + src * cols) + v);
+    reinterpret_cast<uint4 *>(out + i * cols)[v] = __ldg(reinterpret_cast<const uint4 *>(T + src * cols) + v);
   }
 }
-// mode 1: out[p, i] = T[p, idx[i]]   (rows x r)
-__global__ void gather_cols_kernel(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
-                                   const int32_t *__restrict__ idx, int r, uint16_t *out) {
-  const int64_t total = rows * r;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
-       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t p = t / r, i = t - p * r;
-    const int64_t c = idx[i];
+// mode 1: out[p, i] = T[p, idx[i]]   (rows x r_out; columns r .. r_out - 1 are +0)
+__device__ void gather_cols(const uint16_t *__restrict__ T, int64_t rows, int64_t cols, const int32_t *__restrict__ idx,
+                            int r, int r_out, uint16_t *out, int64_t vb, int64_t vg) {
+  const int64_t total = rows * r_out;
+  for (int64_t t = vb * kGatherThreads + threadIdx.x; t < total; t += vg * kGatherThreads) {
+    const int64_t p = t / r_out, i = t - p * r_out;
+    const int64_t c = i < r ? idx[i] : -1;
     out[t] = (c >= 0 && c < cols) ? __ldg(T + p * cols + c) : static_cast<uint16_t>(0);
   }
 }
-// mode 2: out[q, i] = T[idx[i], q]   (cols x r): a 32-column x r tile through shared memory
-__global__ void gather_rows_t_kernel(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
-                                     const int32_t *__restrict__ idx, int r, uint16_t *out) {
-  __shared__ uint16_t tile[256][34];
-  const int64_t q0 = static_cast<int64_t>(blockIdx.x) * 32;
-  for (int t = threadIdx.x; t < r * 32; t += blockDim.x) {
+// mode 2: out[q, i] = T[idx[i], q]   (cols x r_out; columns r .. r_out - 1 are +0): a 32-column x
+// r_out tile through shared memory
+__device__ void gather_rows_t(const uint16_t *__restrict__ T, int64_t rows, int64_t cols, const int32_t *__restrict__ idx,
+                              int r, int r_out, uint16_t *out, int64_t vb, uint16_t *tile /* [256][34] */) {
+  const int64_t q0 = vb * 32;
+  for (int t = threadIdx.x; t < r_out * 32; t += kGatherThreads) {
     const int i = t >> 5, q = t & 31;
-    const int64_t src = idx[i];
-    tile[i][q] = (src >= 0 && src < rows) ? __ldg(T + src * cols + q0 + q) : static_cast<uint16_t>(0);
+    const int64_t src = i < r ? idx[i] : -1;
+    tile[i * 34 + q] = (src >= 0 && src < rows) ? __ldg(T + src * cols + q0 + q) : static_cast<uint16_t>(0);
   }
   __syncthreads();
-  for (int t = threadIdx.x; t < r * 32; t += blockDim.x) {
-    const int q = t / r, i = t - q * r;
-    out[(q0 + q) * r + i] = tile[i][q];
+  for (int t = threadIdx.x; t < r_out * 32; t += kGatherThreads) {
+    const int q = t / r_out, i = t - q * r_out;
+    out[(q0 + q) * r_out + i] = tile[i * 34 + q];
   }
 }
 // mode 2 when cols % 64 == 0 and r % 32 == 0: a CTA moves 64 columns x r selected rows with
 // 16-byte loads into shared memory, then each thread writes r/4 contiguous values of one output
 // row with 16-byte stores (column reads from the tile are conflict-free: consecutive lanes read
 // consecutive columns of one row).
-__global__ void __launch_bounds__(256) gather_rows_t_vec_kernel(const uint16_t *__restrict__ T, int64_t rows,
-                                                                 int64_t cols, const int32_t *__restrict__ idx,
-                                                                 int r, uint16_t *out) {
-  __shared__ __align__(16) uint16_t tile[256][72];
-  const int64_t q0 = static_cast<int64_t>(blockIdx.x) * 64;
-  for (int t = threadIdx.x; t < r * 8; t += blockDim.x) {
+__device__ void gather_rows_t_vec(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
+                                  const int32_t *__restrict__ idx, int r, uint16_t *out, int64_t vb,
+                                  uint16_t *tile /* [256][72], 16-byte aligned */) {
+  const int64_t q0 = vb * 64;
+  for (int t = threadIdx.x; t < r * 8; t += kGatherThreads) {
     const int i = t >> 3, c = t & 7;
     const int64_t src = idx[i];
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (src >= 0 && src < rows) v = __ldg(reinterpret_cast<const uint4 *>(T + src * cols + q0) + c);
-    *reinterpret_cast<uint4 *>(&tile[i][8 * c]) = v;
+    *reinterpret_cast<uint4 *>(&tile[i * 72 + 8 * c]) = v;
   }
   __syncthreads();
   const int q = threadIdx.x & 63, part = threadIdx.x >> 6;   // four parts of r/4 values
@@ -80,20 +82,65 @@ __global__ void __launch_bounds__(256) gather_rows_t_vec_kernel(const uint16_t *
     uint32_t w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      w[k] = static_cast<uint32_t>(tile[ib + 2 * k][q]) | (static_cast<uint32_t>(tile[ib + 2 * k + 1][q]) << 16);
+      w[k] = static_cast<uint32_t>(tile[(ib + 2 * k) * 72 + q]) | (static_cast<uint32_t>(tile[(ib + 2 * k + 1) * 72 + q]) << 16);
     *reinterpret_cast<uint4 *>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 // mode 3: out[i, p] = T[p, idx[i]]   (r x rows)
-__global__ void gather_cols_t_kernel(const uint16_t *__restrict__ T, int64_t rows, int64_t cols,
-                                     const int32_t *__restrict__ idx, int r, uint16_t *out) {
+__device__ void gather_cols_t(const uint16_t *__restrict__ T, int64_t rows, int64_t cols, const int32_t *__restrict__ idx,
+                              int r, uint16_t *out, int64_t vb, int64_t vg) {
   const int64_t total = rows * r;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
-       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  for (int64_t t = vb * kGatherThreads + threadIdx.x; t < total; t += vg * kGatherThreads) {
     const int64_t i = t / rows, p = t - i * rows;
     const int64_t c = idx[i];
     out[t] = (c >= 0 && c < cols) ? __ldg(T + p * cols + c) : static_cast<uint16_t>(0);
   }
+}
+
+unsigned grid_for(int64_t work, int threads, int64_t cap = 8192) {
+  int64_t b = (work + threads - 1) / threads;
+  if (b < 1) b = 1;
+  if (b > cap) b = cap;
+  return static_cast<unsigned>(b);
+}
+
+// The mode-2 variant and the block count of one gather job (r_out already resolved).
+bool rows_t_vec(const GatherJob &j) { return j.cols % 64 == 0 && j.r % 32 == 0 && j.r_out == j.r; }
+int64_t gather_blocks(const GatherJob &j) {
+  switch (j.mode) {
+    case 0: return grid_for(j.r * (j.cols >> 3), kGatherThreads);
+    case 1: return grid_for(j.rows * j.r_out, kGatherThreads);
+    case 2: return rows_t_vec(j) ? j.cols / 64 : j.cols / 32;
+    default: return grid_for(j.rows * j.r, kGatherThreads);
+  }
+}
+
+__device__ __forceinline__ void gather_job(const GatherJob &j, int64_t vb, int64_t vg, uint16_t *tile) {
+  switch (j.mode) {
+    case 0: gather_rows(j.T, j.rows, j.cols, j.idx, j.r, j.out, vb, vg); break;
+    case 1: gather_cols(j.T, j.rows, j.cols, j.idx, j.r, j.r_out, j.out, vb, vg); break;
+    case 2:
+      if (j.cols % 64 == 0 && j.r % 32 == 0 && j.r_out == j.r)
+        gather_rows_t_vec(j.T, j.rows, j.cols, j.idx, j.r, j.out, vb, tile);
+      else
+        gather_rows_t(j.T, j.rows, j.cols, j.idx, j.r, j.r_out, j.out, vb, tile);
+      break;
+    default: gather_cols_t(j.T, j.rows, j.cols, j.idx, j.r, j.out, vb, vg); break;
+  }
+}
+
+// Up to kMaxGatherJobs gathers in one launch: blocks [first[k], first[k + 1]) run job k.
+struct GatherLaunch {
+  GatherJob job[kMaxGatherJobs];
+  int64_t first[kMaxGatherJobs + 1];
+  int count;
+};
+
+__global__ void __launch_bounds__(kGatherThreads) gather_multi_kernel(const __grid_constant__ GatherLaunch g) {
+  __shared__ __align__(16) uint16_t tile[kGatherTileElems];
+  int k = 0;
+  while (k + 1 < g.count && blockIdx.x >= g.first[k + 1]) ++k;
+  gather_job(g.job[k], blockIdx.x - g.first[k], g.first[k + 1] - g.first[k], tile);
 }
 
 // ------------------------------------------------------------------------------- scatter-add
@@ -196,38 +243,32 @@ __global__ void bounded_wait_probe_kernel(uint32_t *status) {
   __syncthreads();
 }
 
-unsigned grid_for(int64_t work, int threads, int64_t cap = 8192) {
-  int64_t b = (work + threads - 1) / threads;
-  if (b < 1) b = 1;
-  if (b > cap) b = cap;
-  return static_cast<unsigned>(b);
-}
-
 }  // namespace
+
+cudaError_t launch_gathers(const GatherJob *jobs, int count, cudaStream_t s) {
+  if (count < 0 || count > kMaxGatherJobs) return cudaErrorInvalidValue;
+  GatherLaunch g{};
+  int64_t blocks = 0;
+  for (int k = 0; k < count; ++k) {
+    if (jobs[k].r == 0) continue;
+    GatherJob j = jobs[k];
+    if (j.r_out == 0 || (j.mode != 1 && j.mode != 2)) j.r_out = j.r;
+    if (j.mode < 0 || j.mode > 3 || j.r > 256 || j.r_out < j.r || j.r_out > 256) return cudaErrorInvalidValue;
+    g.job[g.count] = j;
+    g.first[g.count] = blocks;
+    blocks += gather_blocks(j);
+    ++g.count;
+  }
+  if (g.count == 0) return cudaSuccess;
+  g.first[g.count] = blocks;
+  gather_multi_kernel<<<static_cast<unsigned>(blocks), kGatherThreads, 0, s>>>(g);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather(const uint16_t *T, int64_t rows, int64_t cols, const int32_t *idx, int r,
                           int mode, uint16_t *out, cudaStream_t s) {
-  if (r == 0) return cudaSuccess;
-  switch (mode) {
-    case 0:
-      gather_rows_kernel<<<grid_for(r * (cols >> 3), 256), 256, 0, s>>>(T, rows, cols, idx, r, out);
-      break;
-    case 1:
-      gather_cols_kernel<<<grid_for(rows * r, 256), 256, 0, s>>>(T, rows, cols, idx, r, out);
-      break;
-    case 2:
-      if (cols % 64 == 0 && r % 32 == 0)
-        gather_rows_t_vec_kernel<<<static_cast<unsigned>(cols / 64), 256, 0, s>>>(T, rows, cols, idx, r, out);
-      else
-        gather_rows_t_kernel<<<static_cast<unsigned>(cols / 32), 256, 0, s>>>(T, rows, cols, idx, r, out);
-      break;
-    case 3:
-      gather_cols_t_kernel<<<grid_for(rows * r, 256), 256, 0, s>>>(T, rows, cols, idx, r, out);
-      break;
-    default:
-      return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  const GatherJob j{T, rows, cols, idx, r, mode, out, 0};
+  return launch_gathers(&j, 1, s);
 }
 
 cudaError_t launch_scatter_add(void *C, int64_t P, int64_t Q, int out_dtype, const float *partial,

@@ -55,7 +55,9 @@ def test_workspace_size_validation(lib):
     plan.fwd = 0
     plan.oe_rank = 300
     assert lib.LIB.adahop_workspace_size(C.byref(plan), 4096, 2048, 8192, C.byref(bad)) == 2
-    plan.oe_rank = 12        # not a multiple of 8
+    plan.oe_rank = 12        # any rank 0 .. 256 is accepted
+    assert lib.LIB.adahop_workspace_size(C.byref(plan), 4096, 2048, 8192, C.byref(bad)) == 0
+    plan.oe_rank = -1
     assert lib.LIB.adahop_workspace_size(C.byref(plan), 4096, 2048, 8192, C.byref(bad)) == 2
 
 

@@ -84,9 +84,10 @@ def test_linear_strategies_small(q, gemm, strategy, pset, dtype):
         assert O.rel_frobenius(got, ref["C"]) <= 1e-5
 
 
-@pytest.mark.parametrize("r", [0, 8, 64, 256])
+@pytest.mark.parametrize("r", [0, 1, 8, 13, 50, 64, 256])
 def test_linear_rank_edges(q, r):
-    """r = 0 (plain IHT), r not a multiple of 64, the default 64 and the maximum 256."""
+    """r = 0 (plain IHT), one line, ranks that are not multiples of 8 or 64 (inner slices padded
+    with zero columns), the default 64 and the maximum 256."""
     M, N, K = 512, 256, 384
     X, W, GY = _tensors(M, N, K, 9)
     plan = q.make_plan(O.PAT_COL, O.PAT_NONE, O.PAT_ROW, O.OE_RIGHT, O.OE_LEFT, O.OE_LEFT, r)
@@ -128,7 +129,10 @@ def test_tiny_config(q):
             assert O.rel_frobenius(got, ref["C"]) <= TOL[dtype]
 
 
-def _sampled_parity(q, wl_name, li, n_rows=48, dtype=torch.float32):
+def _sampled_parity(q, wl_name, li, n_rows=48, n_cols=None, dtype=torch.float32):
+    """The three GEMMs of linear `li` of a workload through the C ABI, compared with the oracle on
+    sampled rows (and, with n_cols, sampled columns: the oracle then quantises only the operand
+    lines of that block, so full-size shapes stay quick on the host)."""
     wl = WORKLOADS[wl_name]
     X, W, GY = tensor_recipes(wl, li, device="cuda")
     M, K = X.shape
@@ -148,14 +152,20 @@ def _sampled_parity(q, wl_name, li, n_rows=48, dtype=torch.float32):
     rng = np.random.default_rng(li)
     strategies = {"fwd": plan.fwd, "dgrad": plan.dgrad, "wgrad": plan.wgrad}
     for gemm, out in (("fwd", Y), ("dgrad", dX), ("wgrad", dW)):
-        P = out.shape[0]
+        P, Qn = out.shape
         rows = np.sort(rng.choice(P, n_rows, replace=False))
+        cols = None if n_cols is None else np.sort(rng.choice(Qn, n_cols, replace=False))
         oe = O.gemm_plan(gemm, strategies[gemm], want["patterns"], plan.oe_rank, {"X": Xb, "W": Wb, "GY": Gb})
         if oe is not None and oe["role"] == "P":
             rows = np.unique(np.concatenate([rows, oe["idx"][:8]]))
+        if oe is not None and oe["role"] == "Q" and cols is not None:
+            cols = np.unique(np.concatenate([cols, oe["idx"][:8]]))
         ref = O.gemm_oracle(gemm, strategies[gemm], Xb, Wb, Gb, patterns=want["patterns"], r=plan.oe_rank,
-                            rows=rows, oe=oe)
-        got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
+                            rows=rows, cols=cols, oe=oe)
+        got = out[torch.from_numpy(rows).cuda()]
+        if cols is not None:
+            got = got[:, torch.from_numpy(cols).cuda()]
+        got = got.float().cpu().numpy().astype(np.float64)
         err = O.rel_frobenius(got, ref["C"])
         assert err <= TOL[dtype], (wl_name, li, gemm, err)
 
@@ -170,8 +180,9 @@ def test_instella_3b_config_sampled(q, li):
     _sampled_parity(q, "instella-3b", li, dtype=torch.bfloat16)
 
 
-@pytest.mark.parametrize("li", [4])
+@pytest.mark.parametrize("li", [1, 4, 6])
 def test_llama_8b_config_sampled(q, li):
-    """Full-size Llama3.1-8B gate projection (M=32768, N=14336, K=4096), the bench's launch
-    configuration, checked on sampled rows of all three GEMMs."""
-    _sampled_parity(q, "llama3.1-8b", li, n_rows=24, dtype=torch.bfloat16)
+    """Full-size Llama3.1-8B linears in the bench's launch configuration, checked on sampled rows
+    of all three GEMMs: k (N = 1024: the J = 1024 dgrad), gate (N = 14336, K = 4096) and down
+    (N = 4096, K = 14336: J = 14336 in Fwd, Q = 14336 in dgrad)."""
+    _sampled_parity(q, "llama3.1-8b", li, n_rows=32, n_cols=96, dtype=torch.bfloat16)

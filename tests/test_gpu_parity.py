@@ -190,6 +190,49 @@ def test_foid_ties_and_duplicates(q):
         assert idx.cpu().numpy().tolist() == O.foid(T, "row", r).tolist()
 
 
+@pytest.mark.parametrize("axis", [0, 1])
+def test_foid_ties_across_chunks_at_scale(q, axis):
+    """32768 lines whose probes tie in three classes (variance 1, 4, 9): the top-r cut falls inside
+    a tied band that straddles stage-1 chunk boundaries (256, 1024 and 2048 lines per chunk for
+    r = 64 / 256), so the merge must break ties to the lower index across runs.  Bit-exact
+    against the oracle and against the set fixed by construction."""
+    L = 32768
+    alt = np.where(np.arange(64) % 2, -1.0, 1.0)
+    probe = np.tile(alt, (L, 1))
+    winners = np.array([7, 9000, 20000, 32767])
+    mid = np.concatenate([np.arange(250, 263), np.arange(1020, 1031), np.arange(2040, 2057),
+                          np.arange(32752, 32760), [4095, 4096, 16383, 16384]])
+    probe[mid] *= 2.0                            # variance 4
+    probe[winners] *= 3.0                        # variance 9
+    bits = O.f32_to_bf16_bits(probe.astype(np.float32))            # L x 64: line l = row l
+    T = bits if axis == 0 else np.ascontiguousarray(bits.T)        # 64 x L: line l = column l
+    dT = dev_bf16_from_bits(T)
+    mid_sorted = np.sort(mid)
+    for r in (1, 4, 33, 40, 64, 77, 256):
+        # by construction: the winners, then the lowest-indexed tied lines of each class in turn
+        base = np.setdiff1d(np.arange(L), np.concatenate([winners, mid]))
+        ranked = np.concatenate([winners, mid_sorted, base])[:r]
+        want = np.sort(ranked)
+        assert np.array_equal(O.foid(T, "row" if axis == 0 else "col", r), want)
+        idx = torch.full((r,), -1, dtype=torch.int32, device="cuda")
+        mask = torch.full(((L + 31) // 32,), -1, dtype=torch.int32, device="cuda")
+        ws = q.new_workspace(q.adahop_foid_workspace_size(L, r))
+        q.adahop_foid(dT, axis, r, idx, mask, ws)
+        torch.cuda.synchronize()
+        assert q.adahop_get_device_status(ws) == 0
+        assert np.array_equal(idx.cpu().numpy(), want), (axis, r)
+        assert np.array_equal(mask.cpu().numpy().view(np.uint32), bitmap(L, want)), (axis, r)
+    # every line tied: the r lowest indices
+    flat = O.f32_to_bf16_bits(np.tile(alt, (L, 1)).astype(np.float32))
+    dflat = dev_bf16_from_bits(flat if axis == 0 else np.ascontiguousarray(flat.T))
+    for r in (64, 256):
+        idx = torch.full((r,), -1, dtype=torch.int32, device="cuda")
+        ws = q.new_workspace(q.adahop_foid_workspace_size(L, r))
+        q.adahop_foid(dflat, axis, r, idx, None, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(idx.cpu().numpy(), np.arange(r)), (axis, r)
+
+
 # ------------------------------------------------------------------------------ calibration
 def test_calibration_classes(q):
     from synthetic import WORKLOADS, tensor_recipes
@@ -212,7 +255,10 @@ def _rel(got, ref):
     return O.rel_frobenius(got, ref)
 
 
-@pytest.mark.parametrize("P,Q,J", [(128, 256, 256), (256, 512, 384), (384, 384, 1024), (128, 128, 128)])
+# J <= 2048 and J > 2048 run different pipeline configurations of the kernel (2304: an odd
+# multiple of 128, whose last slice is half full)
+@pytest.mark.parametrize("P,Q,J", [(128, 256, 256), (256, 512, 384), (384, 384, 1024), (128, 128, 128),
+                                   (256, 384, 2304), (384, 256, 4096)])
 @pytest.mark.parametrize("r", [0, 16, 64, 128])
 @pytest.mark.parametrize("out", ["fp32", "bf16"])
 def test_gemm_mxfp4_against_oracle(q, P, Q, J, r, out):
@@ -273,6 +319,58 @@ def test_gemm_bf16_split_partials(q, J, S):
 
 
 # ------------------------------------------------------------------------------ scatter-add
+# (P or Q, the other dimension, J): the cluster's split count runs through 1, 2, 4 and 8
+@pytest.mark.parametrize("axis,other,J,b_kmajor", [
+    (0, 256, 128, 1), (0, 512, 512, 0), (0, 256, 2048, 1), (0, 4096, 2048, 0),
+    (1, 320, 256, 1), (1, 1024, 4096, 1), (1, 384, 1024, 0)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gemm_bf16_scatter_add(q, axis, other, J, b_kmajor, dtype):
+    """The outer-OE outlier GEMM with the scatter-add fused: C[idx, :] += A . B (axis 0) or
+    C[:, idx] += A . B (axis 1) against the float64 product added to C's previous values; every
+    other element of C is left bit for bit as it was."""
+    r = 64
+    rng = np.random.default_rng(J + other + axis)
+    if axis == 0:
+        P, Q = r, other
+        c_rows, c_cols = 1024, Q
+        idx = np.sort(rng.choice(c_rows, r, replace=False)).astype(np.int32)
+    else:
+        P, Q = other, r
+        c_rows, c_cols = P, 768
+        idx = np.sort(rng.choice(c_cols, r, replace=False)).astype(np.int32)
+    A = _bits((P, J), 3, std=1.0)                            # K-major: P x J
+    B = _bits((Q, J) if b_kmajor else (J, Q), 4, std=0.05)   # K-major Q x J, or stored J x Q
+    C0 = torch.randn((c_rows, c_cols), generator=torch.Generator().manual_seed(5)).to(dtype)
+    C = C0.cuda()
+    ws = q.new_workspace(256)
+    q.adahop_gemm_bf16_scatter_add(dev_bf16_from_bits(A), 1, dev_bf16_from_bits(B), b_kmajor, P, Q, J, C,
+                                   torch.from_numpy(idx).cuda(), r, axis, ws)
+    torch.cuda.synchronize()
+    assert q.adahop_get_device_status(ws) == 0
+    f = lambda b: O.bf16_to_f32(b).astype(np.float64)
+    prod = f(A) @ (f(B).T if b_kmajor else f(B))             # P x Q
+    got = C.float().cpu().numpy().astype(np.float64)
+    before = C0.float().numpy().astype(np.float64)
+    want = before.copy()
+    if axis == 0:
+        want[idx, :] += prod
+        touched = np.zeros(c_rows, bool)
+        touched[idx] = True
+        assert np.array_equal(got[~touched], before[~touched])
+        err = O.rel_frobenius(got[idx] - before[idx], want[idx] - before[idx])
+    else:
+        want[:, idx] += prod
+        touched = np.zeros(c_cols, bool)
+        touched[idx] = True
+        assert np.array_equal(got[:, ~touched], before[:, ~touched])
+        err = O.rel_frobenius(got[:, idx] - before[:, idx], want[:, idx] - before[:, idx])
+    # the added part, measured against the exact product: one float32 sum, one rounding of C
+    tol = TOL_FP32 if dtype == torch.float32 else 2e-2
+    assert err <= tol, err
+    if dtype == torch.float32:
+        assert O.rel_frobenius(got, want) <= 1e-5
+
+
 @pytest.mark.parametrize("axis", [0, 1])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_scatter_add(q, axis, dtype):

@@ -10,7 +10,8 @@ import numpy as np
 import pytest
 import torch
 
-from synthetic import normal_bf16
+import oracle as O
+from synthetic import bf16_bits, normal_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -47,6 +48,8 @@ def test_noalloc_foid_matches_workspace_foid_on_two_calls_in_a_row(q):
         assert np.array_equal(idx, idx_ref)
         assert np.array_equal(mask, mask_ref)
         assert len(np.unique(idx)) == r and np.all(np.diff(idx) > 0)
+        # and directly against the CPU oracle's FOID (appendix FOID paragraph), bit for bit
+        assert np.array_equal(idx, O.foid(bf16_bits(T), "row" if axis == 0 else "col", r))
 
 
 def test_noalloc_foid_rejects_requests_beyond_its_scratch(q):
