@@ -220,8 +220,8 @@ def launches_per_gemm(gemm: str, strategy: int, r: int, pats: dict, foid_shared:
         role = _AXIS_ROLE[gemm][t][axis]
         foid = 0 if foid_shared else 1       # one launch: local top-r, the last CTA merges
         gath = 0 if pre_gathered else 1      # this GEMM's outlier slices in one launch
-        # quantise A, B; inner: fused GEMM; outer: GEMM + BF16 outlier GEMM + scatter-add
-        return foid + 2 + gath + (1 if role == "J" else 3)
+        # quantise A, B; inner: fused GEMM; outer: GEMM + the BF16 outlier GEMM with the scatter-add
+        return foid + 2 + gath + (1 if role == "J" else 2)
     return 3                                 # quantise A, quantise B, GEMM
 
 

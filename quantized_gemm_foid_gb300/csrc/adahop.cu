@@ -275,8 +275,9 @@ adahop_status bf16_scatter_gemm(const Ctx &cx, const void *A, int a_kmajor, cons
     ST_TRY(make_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, J, P, 64, 128));
   else
     ST_TRY(make_map(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, P, J, 64, 64));
+  // 128 x 128 output tiles: B boxes of 128 rows (K-major) or two 64-column boxes (MN-major)
   if (b_kmajor)
-    ST_TRY(make_map(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, J, Q, 64, 256));
+    ST_TRY(make_map(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, J, Q, 64, 128));
   else
     ST_TRY(make_map(&maps.b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, Q, J, 64, 64));
   maps.ao = maps.a;

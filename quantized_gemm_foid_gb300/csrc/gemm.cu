@@ -93,6 +93,22 @@ struct Bf16Cfg {
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
 };
 
+// kind 2 (the outlier GEMM with the fused scatter-add): 128 x 128 tiles, so that a product with
+// few output tiles still spreads over many clusters of few CTAs (a wave of clusters must fit the
+// GPU at once; clusters of 8 fit only 15 times on a 152-SM part).
+struct ScatterCfg {
+  static constexpr int kBM = 128;
+  static constexpr int kBN = 128;
+  static constexpr int kStages = 6;
+  static constexpr int kBK = 64;
+  static constexpr uint32_t kABytes = 128 * 128;   // 16 KB
+  static constexpr uint32_t kBBytes = kBN * 128;   // 16 KB
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = 128;
+  static constexpr uint32_t kPartialRowBytes = kBN * 4 + 16;   // padded: conflict-free 16-byte row writes
+  static_assert(kBM * kPartialRowBytes <= kStages * kStageBytes, "the partial tile must fit the stage buffers");
+};
+
 template <int STAGES>
 struct SmemCtl {
   uint64_t full[STAGES];
@@ -680,7 +696,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // in float32 and rounds once to C's type: C[idx[i], q] += O[i, q] (axis 0) or C[p, idx[i]] +=
 // O[p, i] (axis 1).  A second cluster barrier keeps every partial alive until all are read.
 // =============================================================================================
-constexpr uint32_t kPartialRowBytes = 256 * 4 + 16;   // padded: conflict-free 16-byte row writes
 
 __device__ __forceinline__ void scatter_add4(const GemmArgs &g, int64_t row, int64_t col, const float4 &o) {
   const float add[4] = {o.x, o.y, o.z, o.w};
@@ -719,7 +734,7 @@ __device__ __forceinline__ void scatter_add4(const GemmArgs &g, int64_t row, int
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_scatter_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
-  using C = Bf16Cfg;
+  using C = ScatterCfg;
   extern __shared__ uint8_t smem_raw[];
   __shared__ SmemCtl<C::kStages> ctl;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // swizzle atoms need alignment
@@ -729,8 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t nsplit = cluster_nctarank();
   const int64_t tile = blockIdx.x / nsplit;
   const int num_k = static_cast<int>((g.J + C::kBK - 1) / C::kBK);
-  const int64_t tiles_n = (g.Q + BN - 1) / BN;
-  const int64_t m0 = (tile / tiles_n) * C::kBM, n0 = (tile % tiles_n) * BN;
+  const int64_t tiles_n = (g.Q + C::kBN - 1) / C::kBN;
+  const int64_t m0 = (tile / tiles_n) * C::kBM, n0 = (tile % tiles_n) * C::kBN;
   const int per = (num_k + static_cast<int>(nsplit) - 1) / static_cast<int>(nsplit);
   const int k_begin = min(num_k, static_cast<int>(split) * per);
   const int k_end = min(num_k, k_begin + per);
@@ -746,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl.tmem_base), 256);
+    tmem_alloc(smem_u32(&ctl.tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -784,7 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (g.b_mn_major) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * 8192, &maps.b, full, static_cast<int32_t>(n0 + 64 * c), k0);
+          for (int c = 0; c < C::kBN / 64; ++c)
+            tma_load_2d(sB + c * 8192, &maps.b, full, static_cast<int32_t>(n0 + 64 * c), k0);
         } else {
           tma_load_2d(sB, &maps.b, full, k0, static_cast<int32_t>(n0));
         }
@@ -804,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    const uint32_t idesc = make_idesc_bf16(C::kBM, BN, g.a_mn_major != 0, g.b_mn_major != 0);
+    const uint32_t idesc = make_idesc_bf16(C::kBM, C::kBN, g.a_mn_major != 0, g.b_mn_major != 0);
     for (int ks = k_begin; ks < k_end; ++ks) {
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag))) {
         ok = false;
@@ -842,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------------ partial -> shared memory
     // The pipeline is drained once the accumulator is ready (every MMA, hence every operand load,
-    // has completed), so the stage buffers hold the partial tile: 128 rows of 256 floats.
+    // has completed), so the stage buffers hold the partial tile: 128 rows of 128 floats.
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     bool ready = true;
@@ -857,18 +873,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       tc_fence_after();
-      const uint32_t row_addr = smem_base + static_cast<uint32_t>(32 * quad + lane) * kPartialRowBytes;
+      const uint32_t row_addr = smem_base + static_cast<uint32_t>(32 * quad + lane) * C::kPartialRowBytes;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < C::kBN / 64; ++j) {                 // this warp's half: BN / 2 columns
         uint32_t v[32];
         if (k_end > k_begin) {
-          tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + 128u * half + 32u * j, v);
+          tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + (C::kBN / 2) * half + 32u * j, v);
           tmem_wait_ld();
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0u;             // an empty J range adds zeros
         }
-        const uint32_t a = row_addr + (128u * half + 32u * j) * 4u;
+        const uint32_t a = row_addr + ((C::kBN / 2) * half + 32u * j) * 4u;
 #pragma unroll
         for (int q = 0; q < 8; ++q) st_shared_v4(a + 16u * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       }
@@ -884,13 +900,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!any_abort) {
       const int te = threadIdx.x - 64;                        // 256 reducing threads
       const int rows_per = C::kBM / static_cast<int>(nsplit);
-      const int items = rows_per * (BN / 4);
+      const int items = rows_per * (C::kBN / 4);
       for (int it = te; it < items; it += kEpiWarps * 32) {
-        const int rr = static_cast<int>(split) * rows_per + it / (BN / 4);
-        const int c4 = it % (BN / 4);
+        const int rr = static_cast<int>(split) * rows_per + it / (C::kBN / 4);
+        const int c4 = it % (C::kBN / 4);
         const int64_t row = m0 + rr, col = n0 + 4 * c4;
         if (row >= g.P || col >= g.Q) continue;
-        const uint32_t off = smem_base + static_cast<uint32_t>(rr) * kPartialRowBytes + 16u * c4;
+        const uint32_t off = smem_base + static_cast<uint32_t>(rr) * C::kPartialRowBytes + 16u * c4;
         float4 acc = ld_cluster_v4(cluster_map(off, 0));
         for (uint32_t k = 1; k < nsplit; ++k) {
           const float4 o = ld_cluster_v4(cluster_map(off, k));
@@ -906,7 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   }
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // attr must hold two entries: the cluster shape and programmatic dependent launch (pdl_enter).
@@ -981,35 +997,66 @@ cudaError_t launch_bf16(const GemmArgs &g, const GemmMaps &maps, int num_sms, cu
   return cudaGetLastError();
 }
 
-int scatter_splits(int64_t P, int64_t Q, int64_t J, int num_sms) {
-  const int64_t tiles = ((P + Bf16Cfg::kBM - 1) / Bf16Cfg::kBM) * ((Q + BN - 1) / BN);
-  const int64_t k_stages = (J + Bf16Cfg::kBK - 1) / Bf16Cfg::kBK;
-  int s = 1;
-  while (s < 8 && tiles * (2 * s) <= num_sms && k_stages >= 4 * (2 * s)) s *= 2;
-  return s;
-}
+size_t scatter_smem_bytes() { return ScatterCfg::kStages * ScatterCfg::kStageBytes + 1024; }
 
-cudaError_t launch_bf16_scatter(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
-  const size_t smem = gemm_smem_bytes(1);
-  static_assert(Bf16Cfg::kBM * kPartialRowBytes <= Bf16Cfg::kStages * Bf16Cfg::kStageBytes,
-                "the partial tile must fit the stage buffers");
-  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  const int splits = scatter_splits(g.P, g.Q, g.J, num_sms);
-  const int64_t tiles = ((g.P + Bf16Cfg::kBM - 1) / Bf16Cfg::kBM) * ((g.Q + BN - 1) / BN);
-  cudaLaunchAttribute attr[1];
+cudaLaunchConfig_t scatter_launch_config(cudaLaunchAttribute *attr, unsigned grid, int splits, cudaStream_t s) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles * splits), 1, 1);
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = scatter_smem_bytes();
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Clusters of `splits` CTAs of the outlier GEMM that fit the current device at once (cached per
+// device and size).
+int64_t scatter_cluster_capacity(int splits) {
+  constexpr int kMaxDevices = 64;
+  static int64_t cached[kMaxDevices][4] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  const int slot = splits == 1 ? 0 : splits == 2 ? 1 : splits == 4 ? 2 : 3;
+  if (cached[dev][slot] > 0) return cached[dev][slot];
+  if (cudaFuncSetAttribute(gemm_bf16_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(scatter_smem_bytes())) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = scatter_launch_config(attr, static_cast<unsigned>(splits * 8), splits, 0);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_bf16_scatter_kernel, &cfg) != cudaSuccess || clusters <= 0) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cached[dev][slot] = clusters;
+  return clusters;
+}
+
+// The J split (cluster size): the largest of 8, 4, 2 that keeps at least four 64-wide J stages
+// per CTA, no more CTAs than SMs, and every cluster resident in one wave; else 1.
+int scatter_splits(int64_t P, int64_t Q, int64_t J, int num_sms) {
+  const int64_t tiles = ((P + ScatterCfg::kBM - 1) / ScatterCfg::kBM) * ((Q + ScatterCfg::kBN - 1) / ScatterCfg::kBN);
+  const int64_t k_stages = (J + ScatterCfg::kBK - 1) / ScatterCfg::kBK;
+  for (int s = 8; s >= 2; s >>= 1)
+    if (tiles * s <= num_sms && k_stages >= 4 * s && tiles <= scatter_cluster_capacity(s)) return s;
+  return 1;
+}
+
+cudaError_t launch_bf16_scatter(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(scatter_smem_bytes()));
+  if (e != cudaSuccess) return e;
+  const int splits = scatter_splits(g.P, g.Q, g.J, num_sms);
+  const int64_t tiles = ((g.P + ScatterCfg::kBM - 1) / ScatterCfg::kBM) * ((g.Q + ScatterCfg::kBN - 1) / ScatterCfg::kBN);
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = scatter_launch_config(attr, static_cast<unsigned>(tiles * splits), splits, s);
   e = cudaLaunchKernelEx(&cfg, gemm_bf16_scatter_kernel, maps, g);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
