@@ -542,7 +542,7 @@ def host_link_gbs(device, nbytes: int = 1 << 30) -> dict:
 
 
 # ------------------------------------------------------------------------------------ peak probes (K8)
-def pipe_probe(q, kind: int = 1, sf_copies: int = 1, reps: int = 3, iters: int = 20000) -> dict:
+def pipe_probe(q, kind: int = 1, sf_copies: int = 1, reps: int = 3, iters: int = 20000, n: int = 256) -> dict:
     """The tensor pipe's own rate for one MMA kind (K8: back-to-back tcgen05.mma on resident
     shared-memory operands, one CTA per SM).  Default: kind::mxf4 with the six scale-factor copies
     the fused GEMM issues per 256-wide J slice.  Median of `reps` launches: FLOP per clock per SM
@@ -550,10 +550,10 @@ def pipe_probe(q, kind: int = 1, sf_copies: int = 1, reps: int = 3, iters: int =
     ctas = q.adahop_probe_ctas()
     out = torch.zeros(3 * ctas, dtype=torch.int64, device="cuda")
     ws = q.new_workspace(256)
-    flop = 4 * 2 * 128 * 256 * q.MMA_K_PER_INSTR[kind] * iters
+    flop = 4 * 2 * 128 * n * q.MMA_K_PER_INSTR[kind] * iters
     per_clk, mhz, tflops = [], [], []
     for _ in range(reps):
-        q.adahop_probe_mma_rate(kind, sf_copies, iters, out, ws)
+        q.adahop_probe_mma_rate(kind, sf_copies, iters, out, ws, n=n)
         torch.cuda.synchronize()
         if q.adahop_get_device_status(ws) != 0:
             raise SystemExit("mma rate probe: a bounded wait ran out")
@@ -561,7 +561,8 @@ def pipe_probe(q, kind: int = 1, sf_copies: int = 1, reps: int = 3, iters: int =
         per_clk.append(float((flop / rec[:, 0]).median()))
         mhz.append(float((rec[:, 0] / (rec[:, 2] - rec[:, 1])).median()) * 1e3)
         tflops.append(flop * ctas / (float(rec[:, 2].max() - rec[:, 1].min()) / 1e9) / 1e12)
-    return {"kind": q.MMA_KIND_NAMES[kind] + (" + per-slice scale copies" if sf_copies and kind else ""),
+    return {"kind": q.MMA_KIND_NAMES[kind] + (" + per-slice scale copies" if sf_copies and kind else "")
+            + ("" if n == 256 else f", N = {n}"),
             "flop_per_clk_per_sm": round(statistics.median(per_clk), 1), "sms": ctas,
             "sm_mhz": round(statistics.median(mhz), 1), "tflops": round(statistics.median(tflops), 1)}
 
@@ -602,6 +603,9 @@ def peaks_report(q, device) -> dict:
     rates = {}
     for kind, sf in ((0, 0), (1, 0), (1, 1), (2, 0), (2, 1), (3, 0)):
         rates[f"{q.MMA_KIND_NAMES[kind]}{' +sf' if sf else ''}"] = pipe_probe(q, kind, sf)
+    # a 128-wide MMA takes half as long: can one lane still issue four MMAs and their copies?
+    for kind, sf in ((0, 0), (1, 0), (1, 1)):
+        rates[f"{q.MMA_KIND_NAMES[kind]}{' +sf' if sf else ''} N=128"] = pipe_probe(q, kind, sf, n=128)
     return {"mma": rates, "copy_gbs": copy_probe(q, device)}
 
 

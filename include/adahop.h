@@ -317,19 +317,20 @@ adahop_status adahop_calibration_stats(const void *T, int64_t rows, int64_t cols
 int adahop_probe_ctas(void);
 
 /* Tensor-pipe rate probe.  One CTA per SM; in each, one elected lane issues `iters` groups of
- * four back-to-back tcgen05.mma instructions (cta_group::1, M = 128, N = 256) on operands that
+ * four back-to-back tcgen05.mma instructions (cta_group::1, M = 128, N = n: 128 or 256) on operands that
  * stay in shared memory, all accumulating into one tensor-memory tile, then waits (bounded) for
  * them to finish.  kind: 0 = kind::f16 (bf16 x bf16, K = 16 per instruction); 1 = kind::mxf4,
  * scale_vec::2X; 2 = kind::mxf4nvf4, scale_vec::2X; 3 = kind::mxf4nvf4, scale_vec::4X (kinds 1-3:
  * E2M1 operands, UE8M0 scales, K = 64).  sf_copies = 1 adds, per group, the six scale-factor
- * copies (tcgen05.cp) the fused MXFP4 GEMM issues per 256-wide slice of J (kinds 1-3 only).
+ * copies (tcgen05.cp) the fused MXFP4 GEMM issues per 256-wide slice of J (kinds 1-3 only; with
+ * n = 128 the B copies cover 128 rows: four copies per group).
  * Operand values are a fixed pattern; nothing but timing is produced.
  * out: device, 16-byte aligned, out_bytes >= 24 * adahop_probe_ctas(); CTA c writes
  * out[3c] = clock64 cycles of its loop, out[3c+1] / out[3c+2] = %globaltimer ns at its start /
- * end.  FLOP per group: 4 x 2 x 128 x 256 x K.  iters: 1 .. 2^20 (ERR_SHAPE otherwise).
+ * end.  FLOP per group: 4 x 2 x 128 x n x K.  iters: 1 .. 2^20 (ERR_SHAPE otherwise).
  * workspace: >= 256 bytes, 256-byte aligned, first 256 bytes zeroed (status word; a wait that
  * ran out is reported by adahop_get_device_status).  Asynchronous on `stream`. */
-adahop_status adahop_probe_mma_rate(int kind, int sf_copies, int64_t iters, uint64_t *out, size_t out_bytes,
+adahop_status adahop_probe_mma_rate(int kind, int sf_copies, int n, int64_t iters, uint64_t *out, size_t out_bytes,
                                     void *workspace, size_t ws_bytes, adahop_stream_t stream);
 
 /* Streaming copy probe: dst[0:bytes] = src[0:bytes] with 16-byte loads and stores (streaming

@@ -75,7 +75,7 @@ PROTOTYPES = {
     "adahop_calibration_stats": (c_int, [c_void_p, c_int64, c_int64, c_void_p, c_void_p,
                                          c_void_p]),
     "adahop_probe_ctas": (c_int, []),
-    "adahop_probe_mma_rate": (c_int, [c_int, c_int, c_int64, c_void_p, c_size_t, c_void_p, c_size_t,
+    "adahop_probe_mma_rate": (c_int, [c_int, c_int, c_int, c_int64, c_void_p, c_size_t, c_void_p, c_size_t,
                                       c_void_p]),
     "adahop_probe_copy": (c_int, [c_void_p, c_void_p, c_size_t, c_void_p]),
 }

@@ -287,11 +287,11 @@ def adahop_probe_ctas() -> int:
     return int(LIB.adahop_probe_ctas())
 
 
-def adahop_probe_mma_rate(kind: int, sf_copies: int, iters: int, out, ws, stream=None) -> None:
-    """Launches the tensor-pipe rate probe; `out` is a uint64 (int64) device tensor of at least
-    3 * adahop_probe_ctas() entries (per CTA: loop cycles, start ns, end ns)."""
+def adahop_probe_mma_rate(kind: int, sf_copies: int, iters: int, out, ws, stream=None, n: int = 256) -> None:
+    """Launches the tensor-pipe rate probe (MMA width n = 128 or 256); `out` is a uint64 (int64)
+    device tensor of at least 3 * adahop_probe_ctas() entries (per CTA: loop cycles, start ns, end ns)."""
     _cuda(out, "out")
-    _check(LIB.adahop_probe_mma_rate(int(kind), int(sf_copies), int(iters), _p(out),
+    _check(LIB.adahop_probe_mma_rate(int(kind), int(sf_copies), int(n), int(iters), _p(out),
                                      out.numel() * out.element_size(), _p(ws), ws.numel(), _stream(stream)),
            "adahop_probe_mma_rate")
 

@@ -919,16 +919,17 @@ int adahop_probe_ctas(void) {
   return di.num_sms;
 }
 
-adahop_status adahop_probe_mma_rate(int kind, int sf_copies, int64_t iters, uint64_t *out, size_t out_bytes,
+adahop_status adahop_probe_mma_rate(int kind, int sf_copies, int n, int64_t iters, uint64_t *out, size_t out_bytes,
                                     void *workspace, size_t ws_bytes, adahop_stream_t stream) {
-  if (!out || !workspace || kind < 0 || kind > 3 || (sf_copies != 0 && sf_copies != 1)) return ADAHOP_ERR_INVALID_ARG;
+  if (!out || !workspace || kind < 0 || kind > 3 || (sf_copies != 0 && sf_copies != 1) || (n != 128 && n != 256))
+    return ADAHOP_ERR_INVALID_ARG;
   if (iters < 1 || iters > (int64_t(1) << 20)) return ADAHOP_ERR_SHAPE;
   if (!aligned(out, 16) || !aligned(workspace, 256)) return ADAHOP_ERR_ALIGN;
   if (ws_bytes < 256) return ADAHOP_ERR_WORKSPACE;
   DeviceInfo di;
   ST_TRY(device_info(&di));
   if (out_bytes < 3 * sizeof(uint64_t) * static_cast<size_t>(di.num_sms)) return ADAHOP_ERR_WORKSPACE;
-  CUDA_TRY(launch_mma_rate_probe(kind, sf_copies, iters, out, static_cast<uint32_t *>(workspace), di.num_sms,
+  CUDA_TRY(launch_mma_rate_probe(kind, sf_copies, n, iters, out, static_cast<uint32_t *>(workspace), di.num_sms,
                                  reinterpret_cast<cudaStream_t>(stream)),
            "mma rate probe launch");
   return ADAHOP_OK;

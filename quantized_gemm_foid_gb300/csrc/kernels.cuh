@@ -65,8 +65,9 @@ cudaError_t launch_calib_stats(const uint16_t *T, int64_t rows, int64_t cols, fl
                                float *col_ms, cudaStream_t s);
 
 // K8 peak probes.  kind: 0 kind::f16, 1 kind::mxf4 (2X), 2 kind::mxf4nvf4 (2X), 3 kind::mxf4nvf4
-// (4X); `ctas` CTAs (one per SM) each write {loop cycles, start ns, end ns} to out[3 * cta ..].
-cudaError_t launch_mma_rate_probe(int kind, int sf_copies, int64_t iters, uint64_t *out, uint32_t *status,
+// (4X); n: MMA width 128 or 256; `ctas` CTAs (one per SM) each write {loop cycles, start ns, end ns}
+// to out[3 * cta ..].
+cudaError_t launch_mma_rate_probe(int kind, int sf_copies, int n, int64_t iters, uint64_t *out, uint32_t *status,
                                   int ctas, cudaStream_t s);
 cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, int num_sms, cudaStream_t s);
 

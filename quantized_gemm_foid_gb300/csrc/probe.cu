@@ -53,9 +53,11 @@ __device__ __forceinline__ void mma_mxf4nvf4_4x(uint32_t d_tmem, uint64_t a_desc
 }
 
 // KIND: 0 = kind::f16 (bf16 x bf16, K = 16); 1 = kind::mxf4 scale_vec::2X; 2 = kind::mxf4nvf4
-// scale_vec::2X; 3 = kind::mxf4nvf4 scale_vec::4X (both with UE8M0 scales; K = 64).
+// scale_vec::2X; 3 = kind::mxf4nvf4 scale_vec::4X (both with UE8M0 scales; K = 64).  N: 256 or 128
+// (with N = 128 each group's MMAs take half the time, so the issuing lane has half as long to
+// issue the same group; SF_COPIES then copies one B atom per 128 B rows, as a 128-wide tile needs).
 // out[3 * cta + 0..2] = loop cycles, start ns, end ns.
-template <int KIND, bool SF_COPIES>
+template <int KIND, bool SF_COPIES, int N>
 __global__ void __launch_bounds__(kProbeThreads, 1)
     mma_rate_kernel(int64_t iters, uint64_t *out, uint32_t *status) {
   extern __shared__ uint8_t smem_raw[];
@@ -108,23 +110,24 @@ __global__ void __launch_bounds__(kProbeThreads, 1)
             const int ka = kk >> 1;
             tmem_cp_32x128b_x4(sfa + 4 * ka, make_smem_desc(base + kProbeSF + 512 * ka, 0, 128, kLayoutNone));
             tmem_cp_32x128b_x4(sfb + 8 * ka, make_smem_desc(base + kProbeSF + 1024 + 512 * ka, 0, 128, kLayoutNone));
-            tmem_cp_32x128b_x4(sfb + 8 * ka + 4,
-                               make_smem_desc(base + kProbeSF + 2048 + 512 * ka, 0, 128, kLayoutNone));
+            if constexpr (N == 256)
+              tmem_cp_32x128b_x4(sfb + 8 * ka + 4,
+                                 make_smem_desc(base + kProbeSF + 2048 + 512 * ka, 0, 128, kLayoutNone));
           }
           const uint64_t adesc = make_smem_desc(base + kProbeA + 32 * kk, 16, 1024, kLayoutSw128);
           const uint64_t bdesc = make_smem_desc(base + kProbeB + 32 * kk, 16, 1024, kLayoutSw128);
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
           const uint32_t sa = sfa + 4 * (kk >> 1), sb = sfb + 8 * (kk >> 1);
           if constexpr (KIND == 0) {
-            mma_bf16(tmem, adesc, bdesc, make_idesc_bf16(128, 256, false, false), acc);
+            mma_bf16(tmem, adesc, bdesc, make_idesc_bf16(128, N, false, false), acc);
           } else if constexpr (KIND == 1) {
-            mma_mxf4(tmem, adesc, bdesc, (kk & 1) ? make_idesc_mxf4(128, 256, 2, 2) : make_idesc_mxf4(128, 256, 0, 0),
+            mma_mxf4(tmem, adesc, bdesc, (kk & 1) ? make_idesc_mxf4(128, N, 2, 2) : make_idesc_mxf4(128, N, 0, 0),
                      sa, sb, acc);
           } else if constexpr (KIND == 2) {
             mma_mxf4nvf4_2x(tmem, adesc, bdesc,
-                            (kk & 1) ? make_idesc_mxf4(128, 256, 2, 2) : make_idesc_mxf4(128, 256, 0, 0), sa, sb, acc);
+                            (kk & 1) ? make_idesc_mxf4(128, N, 2, 2) : make_idesc_mxf4(128, N, 0, 0), sa, sb, acc);
           } else {
-            mma_mxf4nvf4_4x(tmem, adesc, bdesc, make_idesc_mxf4(128, 256, 0, 0), sa, sb, acc);
+            mma_mxf4nvf4_4x(tmem, adesc, bdesc, make_idesc_mxf4(128, N, 0, 0), sa, sb, acc);
           }
         }
       }
@@ -165,28 +168,36 @@ __global__ void __launch_bounds__(256) copy_probe_kernel(const uint4 *__restrict
   for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
 }
 
-template <int KIND, bool SF_COPIES>
+template <int KIND, bool SF_COPIES, int N>
 cudaError_t launch_rate(int64_t iters, uint64_t *out, uint32_t *status, int ctas, cudaStream_t s) {
-  auto *k = mma_rate_kernel<KIND, SF_COPIES>;
+  auto *k = mma_rate_kernel<KIND, SF_COPIES, N>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kProbeSmem));
   if (e != cudaSuccess) return e;
   k<<<ctas, kProbeThreads, kProbeSmem, s>>>(iters, out, status);
   return cudaGetLastError();
 }
 
+template <int N>
+cudaError_t launch_rate_n(int kind, int sf_copies, int64_t iters, uint64_t *out, uint32_t *status, int ctas,
+                          cudaStream_t s) {
+  switch (kind * 2 + (sf_copies ? 1 : 0)) {
+    case 0: case 1: return launch_rate<0, false, N>(iters, out, status, ctas, s);
+    case 2: return launch_rate<1, false, N>(iters, out, status, ctas, s);
+    case 3: return launch_rate<1, true, N>(iters, out, status, ctas, s);
+    case 4: return launch_rate<2, false, N>(iters, out, status, ctas, s);
+    case 5: return launch_rate<2, true, N>(iters, out, status, ctas, s);
+    case 6: return launch_rate<3, false, N>(iters, out, status, ctas, s);
+    case 7: return launch_rate<3, true, N>(iters, out, status, ctas, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
-cudaError_t launch_mma_rate_probe(int kind, int sf_copies, int64_t iters, uint64_t *out, uint32_t *status,
+cudaError_t launch_mma_rate_probe(int kind, int sf_copies, int n, int64_t iters, uint64_t *out, uint32_t *status,
                                   int ctas, cudaStream_t s) {
-  switch (kind * 2 + (sf_copies ? 1 : 0)) {
-    case 0: case 1: return launch_rate<0, false>(iters, out, status, ctas, s);
-    case 2: return launch_rate<1, false>(iters, out, status, ctas, s);
-    case 3: return launch_rate<1, true>(iters, out, status, ctas, s);
-    case 4: return launch_rate<2, false>(iters, out, status, ctas, s);
-    case 5: return launch_rate<2, true>(iters, out, status, ctas, s);
-    case 6: return launch_rate<3, false>(iters, out, status, ctas, s);
-    case 7: return launch_rate<3, true>(iters, out, status, ctas, s);
-  }
+  if (n == 128) return launch_rate_n<128>(kind, sf_copies, iters, out, status, ctas, s);
+  if (n == 256) return launch_rate_n<256>(kind, sf_copies, iters, out, status, ctas, s);
   return cudaErrorInvalidValue;
 }
 

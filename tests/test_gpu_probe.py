@@ -14,20 +14,21 @@ def q():
     return q
 
 
-@pytest.mark.parametrize("kind,sf_copies", [(0, 0), (1, 0), (1, 1), (2, 0), (2, 1), (3, 0)])
-def test_mma_rate_probe(q, kind, sf_copies):
+@pytest.mark.parametrize("kind,sf_copies,n", [(0, 0, 256), (1, 0, 256), (1, 1, 256), (2, 0, 256), (2, 1, 256),
+                                              (3, 0, 256), (0, 0, 128), (1, 1, 128)])
+def test_mma_rate_probe(q, kind, sf_copies, n):
     ctas = q.adahop_probe_ctas()
     assert ctas > 0
     out = torch.zeros(3 * ctas, dtype=torch.int64, device="cuda")
     ws = q.new_workspace(256)
     iters = 2000
-    q.adahop_probe_mma_rate(kind, sf_copies, iters, out, ws)
+    q.adahop_probe_mma_rate(kind, sf_copies, iters, out, ws, n=n)
     assert q.adahop_get_device_status(ws) == 0
     rec = out.view(ctas, 3).cpu()
     cycles = rec[:, 0].double()
     assert bool((cycles > 0).all())
     assert bool((rec[:, 2] > rec[:, 1]).all())
-    flop = 4 * 2 * 128 * 256 * q.MMA_K_PER_INSTR[kind] * iters
+    flop = 4 * 2 * 128 * n * q.MMA_K_PER_INSTR[kind] * iters
     per_clk = flop / cycles
     # the dense tensor pipe of one SM does between 2^11 and 2^17 FLOP per clock for these kinds;
     # anything outside means the probe did not run the MMAs it claims
@@ -43,6 +44,8 @@ def test_mma_rate_probe_rejects_bad_arguments(q):
         q.adahop_probe_mma_rate(1, 0, 0, out, ws)
     with pytest.raises(q.AdahopError):
         q.adahop_probe_mma_rate(1, 0, 10, out[:3], ws)
+    with pytest.raises(q.AdahopError):
+        q.adahop_probe_mma_rate(1, 0, 10, out, ws, n=64)
 
 
 def test_copy_probe(q):
