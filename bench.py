@@ -1020,7 +1020,7 @@ def profile(q, device, args):
         # the fused GEMM on each of the step's 21 shapes, one shape's operands on the device at a
         # time (at most ~1.5 GB), two launches each (for a one-pass DRAM-byte capture per launch)
         wl = WORKLOADS[WORKLOAD]
-        ws = q.new_workspace(4096, device=device)
+        ws = q.new_workspace(q.adahop_gemm_mxfp4_workspace_size(), device=device)   # stream-K where it applies
         n = 0
         for lin in wl.linears:
             M, N, K = wl.M, lin.N, lin.K

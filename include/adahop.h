@@ -26,9 +26,12 @@
  *     number of lines it is drawn from.  Device pointers must be 16-byte aligned and the
  *     workspace 256-byte aligned; otherwise ADAHOP_ERR_ALIGN.
  *   - Inputs must be finite; results for NaN/Inf inputs are unspecified.
- *   - A workspace must start with its first 256 bytes zeroed (the status word lives there).
- *     A device-side failure (a bounded wait that ran out) is recorded in that status word;
- *     adahop_get_device_status() reports and clears it.
+ *   - A workspace of the linear calls must start with its first 16384 bytes zeroed: the status
+ *     word lives there, with the completion counters of FOID and of the fused GEMM's stream-K
+ *     tiles; every call that completes leaves them zero, so a workspace is reused as it is.
+ *     A device-side failure (a bounded wait that ran out) is recorded in the status word;
+ *     adahop_get_device_status() reports and clears it (after such a failure, zero the header
+ *     again before reusing the workspace).
  */
 #ifndef ADAHOP_H
 #define ADAHOP_H
@@ -105,7 +108,8 @@ adahop_status adahop_workspace_size(const adahop_plan *plan, int64_t M, int64_t 
  * axis; pattern = None if both rho < tau, else Column-wise if rho_col >= rho_row, else
  * Row-wise.  The strategy of each GEMM is looked up from its pattern pair:
  *   CN, NN -> IHT; RC, RN -> OE-Left; NC -> OE-Right; CC, RR, NR, CR -> BF16.
- * SYNCHRONOUS: waits for the stream (it copies the statistics to the host).
+ * SYNCHRONOUS: waits for the stream (it copies the statistics to the host).  The workspace needs
+ * at least 16384 + 4 x (max(M, N) + max(N, K)) + 256 bytes (adahop_workspace_size() is enough).
  * opt may be NULL (defaults). */
 adahop_status adahop_calibrate(const void *X, const void *W, const void *GY, int64_t M,
                                int64_t N, int64_t K, const adahop_options *opt,
@@ -261,12 +265,20 @@ adahop_status adahop_gather(const void *T, int64_t rows, int64_t cols, const int
  * A: P x J MXFP4 (codes P x J/2, scales in layout 1), B: Q x J likewise.
  * A_o: P x r bf16 and B_o: Q x r bf16 (r-contiguous; both NULL or r = 0 for no outlier term;
  * r a multiple of 8).  C: bf16 or fp32 per out_dtype.  P, Q, J multiples of 128.
- * The workspace only carries the status word (>= 256 bytes). */
+ * Workspace: at least 256 bytes (the status word).  With at least
+ * adahop_gemm_mxfp4_workspace_size() bytes, whose first 16384 bytes are zero at the first call
+ * (every call leaves them zero), the GEMM balances the tiles that a whole round over the SMs would
+ * leave short (stream-K: their J stages are spread over all CTA pairs, partial sums added in a
+ * fixed order); with less it runs whole tiles only.  Both give results within the same bound. */
 adahop_status adahop_gemm_mxfp4(const uint8_t *a_codes, const uint8_t *a_scales,
                                 const uint8_t *b_codes, const uint8_t *b_scales, int64_t P,
                                 int64_t Q, int64_t J, const void *A_o, const void *B_o, int r,
                                 void *C, adahop_out_dtype out_dtype, void *workspace, size_t ws_bytes,
                                 adahop_stream_t stream);
+
+/* Workspace bytes that let adahop_gemm_mxfp4 use stream-K (a zeroed 16 KB header and one
+ * 256 x 256 float32 partial tile per CTA pair). */
+size_t adahop_gemm_mxfp4_workspace_size(void);
 
 /* BF16 GEMM C (P x Q) = A . B, float32 accumulation (Fig. 5's BF16 path; also the outlier
  * GEMM of outer OE).  a_kmajor 1: A stored P x J (J-contiguous); 0: stored J x P.

@@ -65,6 +65,7 @@ PROTOTYPES = {
     "adahop_gemm_mxfp4": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64,
                                   c_int64, c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p,
                                   c_size_t, c_void_p]),
+    "adahop_gemm_mxfp4_workspace_size": (c_size_t, []),
     "adahop_gemm_bf16": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int64, c_int64, c_int64,
                                  c_void_p, c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "adahop_gemm_bf16_scatter_add": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int64, c_int64, c_int64,

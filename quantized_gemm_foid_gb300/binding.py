@@ -249,6 +249,10 @@ def adahop_gemm_mxfp4(a_codes, a_scales, b_codes, b_scales, P: int, Q: int, J: i
                                  _stream(stream)), "adahop_gemm_mxfp4")
 
 
+def adahop_gemm_mxfp4_workspace_size() -> int:
+    return int(LIB.adahop_gemm_mxfp4_workspace_size())
+
+
 def adahop_gemm_bf16(A, a_kmajor: int, B, b_kmajor: int, P: int, Q: int, J: int, C_out, workspace,
                      splits: int = 1, c_partial=None, out_dtype: int | None = None, stream=None) -> None:
     od = _out_dtype(C_out) if C_out is not None else (OUT_FP32 if out_dtype is None else out_dtype)

@@ -108,10 +108,19 @@ bool dim_ok(int64_t d) { return d > 0 && d % 128 == 0 && d < (int64_t(1) << 31);
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 int round8(int r) { return (r + 7) & ~7; }
 
+// The zeroed header every workspace starts with (zero at the first call; every call that
+// completes leaves it zero): the status word at offset 0, FOID's completion counter at 64, and
+// the fused GEMM's stream-K counters from 1024.
+constexpr size_t kHeaderBytes = 16384;
+constexpr size_t kFoidCounterOffset = 64;
+constexpr size_t kSkCounterOffset = 1024;
+static_assert(kSkCounterOffset + sizeof(uint32_t) * kSkMaxTiles * kSkCountersPerTile <= kHeaderBytes, "header layout");
+constexpr int kSkMaxPairs = 80;   // stream-K partial slots: one per CTA pair (>= 76 pairs on 152 SMs)
+
 // ------------------------------------------------------------------------- workspace layout
 // One GEMM's scratch.  The region sizes are upper bounds over all strategies.
 struct GemmWs {
-  size_t status, foid, idx, mask, a_codes, a_sf, b_codes, b_sf, ao, bo, gath, partial, total;
+  size_t status, foid, idx, mask, a_codes, a_sf, b_codes, b_sf, ao, bo, gath, partial, sk, total;
 };
 
 constexpr int kMaxRank = 256;
@@ -134,7 +143,7 @@ GemmWs gemm_ws(int64_t P, int64_t Q, int64_t J, int r, int num_sms, int64_t line
     return o;
   };
   const int rr = std::max(r, 1);
-  w.status = take(256);
+  w.status = take(kHeaderBytes);
   w.foid = take(foid_scratch_bytes(lines, rr));
   w.idx = take(sizeof(int32_t) * kMaxRank);
   w.mask = take(sizeof(uint32_t) * ((lines + 31) / 32));
@@ -151,6 +160,7 @@ GemmWs gemm_ws(int64_t P, int64_t Q, int64_t J, int r, int num_sms, int64_t line
   const int s_cols = choose_splits((P + 127) / 128, k_stages, num_sms);
   const size_t part = std::max(static_cast<size_t>(s_rows) * rr * Q, static_cast<size_t>(s_cols) * P * rr);
   w.partial = take(part * sizeof(float));
+  w.sk = take(kSkPartialBytesPerPair * kSkMaxPairs);
   w.total = off;
   return w;
 }
@@ -221,18 +231,21 @@ OeChoice oe_choice(int gemm, int strategy, const int pats[3]) {
   return c;
 }
 
-// Inside the workspace's zeroed first 256 bytes: the status word at offset 0 and FOID's completion
-// counter (zero whenever no FOID launch is running: every launch leaves it zero).
-constexpr size_t kFoidCounterOffset = 64;
-
 struct Ctx {
   cudaStream_t s;
   uint8_t *ws;
   GemmWs lay;
   int num_sms;
+  bool sk = false;     // the workspace carries the fused GEMM's stream-K scratch (lay.sk, the header counters)
   uint32_t *status() const { return reinterpret_cast<uint32_t *>(ws + lay.status); }
   uint32_t *foid_counter() const { return reinterpret_cast<uint32_t *>(ws + lay.status + kFoidCounterOffset); }
 };
+// Context of a linear call: its workspace layout always includes the stream-K scratch.
+Ctx linear_ctx(cudaStream_t s, void *workspace, const GemmWs &lay, int num_sms) {
+  Ctx cx{s, static_cast<uint8_t *>(workspace), lay, num_sms};
+  cx.sk = true;
+  return cx;
+}
 
 adahop_status bf16_gemm(const Ctx &cx, const void *A, int a_kmajor, const void *B, int b_kmajor,
                         int64_t P, int64_t Q, int64_t J, void *C, int out_dtype, int splits,
@@ -337,6 +350,11 @@ adahop_status mxf4_gemm(const Ctx &cx, const uint8_t *ac, const uint8_t *asf, co
   g.out_dtype = out_dtype;
   g.splits = 1;
   g.status = cx.status();
+  if (cx.sk) {
+    g.sk_partial = reinterpret_cast<float *>(cx.ws + cx.lay.sk);
+    g.sk_counters = reinterpret_cast<uint32_t *>(cx.ws + cx.lay.status + kSkCounterOffset);
+    g.sk_max_pairs = kSkMaxPairs;
+  }
   CUDA_TRY(launch_gemm(g, maps, cx.num_sms, cx.s), "mxfp4 gemm launch");
   return ADAHOP_OK;
 }
@@ -529,7 +547,7 @@ size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
   }
   b = std::max(b, bwd_gath_layout(M, N, K, r).end);
   // calibration statistics: rows + cols floats of the largest tensor
-  b = std::max(b, align256(256 + sizeof(float) * static_cast<size_t>(std::max(M, N) + std::max(N, K)) + 256));
+  b = std::max(b, align256(kHeaderBytes + sizeof(float) * static_cast<size_t>(std::max(M, N) + std::max(N, K)) + 256));
   return b;
 }
 
@@ -546,7 +564,7 @@ double lower_median_ratio(const std::vector<float> &v) {
 
 adahop_status calibrate_one(const void *T, int64_t rows, int64_t cols, double tau, uint8_t *ws,
                             cudaStream_t s, int *pattern, double *rho_row, double *rho_col) {
-  float *row_ms = reinterpret_cast<float *>(ws + 256);
+  float *row_ms = reinterpret_cast<float *>(ws + kHeaderBytes);
   float *col_ms = row_ms + rows;
   CUDA_TRY(launch_calib_stats(static_cast<const uint16_t *>(T), rows, cols, row_ms, col_ms, s), "calibration stats");
   std::vector<float> hr(rows), hc(cols);
@@ -717,13 +735,13 @@ adahop_status linear_bwd_impl(const adahop_plan *plan, const void *GY, const voi
   uint8_t *sv = const_cast<uint8_t *>(saved);
   const PreA saved_w{sv + sl.w_codes, sv + sl.w_sf}, saved_x{sv + sl.x_codes, sv + sl.x_sf};
   if (dX) {
-    Ctx cx{s, static_cast<uint8_t *>(workspace), ld, di.num_sms};
+    const Ctx cx = linear_ctx(s, workspace, ld, di.num_sms);
     ST_TRY(run_gemm(cx, 1, plan->dgrad, plan->oe_rank, t, pats, dX, out_dtype, share ? &fc : nullptr,
                     dual ? &pre_d : nullptr, sl.has_w ? &saved_w : nullptr, nullptr, nullptr,
                     pre_gath[0] ? &pg[0] : nullptr));
   }
   if (dW) {
-    Ctx cx{s, static_cast<uint8_t *>(workspace), lw, di.num_sms};
+    const Ctx cx = linear_ctx(s, workspace, lw, di.num_sms);
     ST_TRY(run_gemm(cx, 2, plan->wgrad, plan->oe_rank, t, pats, dW, out_dtype, share ? &fc : nullptr,
                     dual ? &pre_w : nullptr, sl.has_x ? &saved_x : nullptr, nullptr, nullptr,
                     pre_gath[1] ? &pg[1] : nullptr));
@@ -779,7 +797,7 @@ adahop_status adahop_calibrate(const void *X, const void *W, const void *GY, int
   ST_TRY(check_shapes(M, N, K));
   if (!aligned(X, 16) || !aligned(W, 16) || (GY && !aligned(GY, 16)) || !aligned(workspace, 256))
     return ADAHOP_ERR_ALIGN;
-  const size_t need = align256(256 + sizeof(float) * static_cast<size_t>(std::max(M, N) + std::max(N, K)) + 256);
+  const size_t need = align256(kHeaderBytes + sizeof(float) * static_cast<size_t>(std::max(M, N) + std::max(N, K)) + 256);
   if (ws_bytes < need) return ADAHOP_ERR_WORKSPACE;
   DeviceInfo di;
   ST_TRY(device_info(&di));
@@ -808,8 +826,8 @@ adahop_status adahop_linear_fwd(const adahop_plan *plan, const void *X, const vo
   DeviceInfo di;
   ST_TRY(linear_common(plan, M, N, K, workspace, ws_bytes, &di));
   const GemmShape sh = shape_of(0, M, N, K);
-  Ctx cx{reinterpret_cast<cudaStream_t>(stream), static_cast<uint8_t *>(workspace),
-         gemm_ws(sh.P, sh.Q, sh.J, plan->oe_rank, kSizingSms, std::max(std::max(M, N), K)), di.num_sms};
+  const Ctx cx = linear_ctx(reinterpret_cast<cudaStream_t>(stream), workspace,
+                            gemm_ws(sh.P, sh.Q, sh.J, plan->oe_rank, kSizingSms, std::max(std::max(M, N), K)), di.num_sms);
   const Tensor t[3] = {{static_cast<const uint16_t *>(X), M, K}, {static_cast<const uint16_t *>(W), N, K}, {nullptr, M, N}};
   const int pats[3] = {plan->x, plan->w, plan->gy};
   return run_gemm(cx, 0, plan->fwd, plan->oe_rank, t, pats, Y, out_dtype, nullptr);
@@ -847,8 +865,8 @@ adahop_status adahop_linear_fwd_save(const adahop_plan *plan, const void *X, con
   if (saved && !aligned(saved, 256)) return ADAHOP_ERR_ALIGN;
   if (saved_bytes < sl.total) return ADAHOP_ERR_WORKSPACE;
   const GemmShape sh = shape_of(0, M, N, K);
-  Ctx cx{reinterpret_cast<cudaStream_t>(stream), static_cast<uint8_t *>(workspace),
-         gemm_ws(sh.P, sh.Q, sh.J, plan->oe_rank, kSizingSms, std::max(std::max(M, N), K)), di.num_sms};
+  const Ctx cx = linear_ctx(reinterpret_cast<cudaStream_t>(stream), workspace,
+                            gemm_ws(sh.P, sh.Q, sh.J, plan->oe_rank, kSizingSms, std::max(std::max(M, N), K)), di.num_sms);
   const Tensor t[3] = {{static_cast<const uint16_t *>(X), M, K}, {static_cast<const uint16_t *>(W), N, K}, {nullptr, M, N}};
   const int pats[3] = {plan->x, plan->w, plan->gy};
   const int r = plan->oe_rank;
@@ -1040,6 +1058,10 @@ adahop_status adahop_gather(const void *T, int64_t rows, int64_t cols, const int
   return ADAHOP_OK;
 }
 
+size_t adahop_gemm_mxfp4_workspace_size(void) {
+  return kHeaderBytes + kSkPartialBytesPerPair * static_cast<size_t>(kSkMaxPairs);
+}
+
 adahop_status adahop_gemm_mxfp4(const uint8_t *a_codes, const uint8_t *a_scales, const uint8_t *b_codes,
                                 const uint8_t *b_scales, int64_t P, int64_t Q, int64_t J, const void *A_o,
                                 const void *B_o, int r, void *C, adahop_out_dtype out_dtype, void *workspace, size_t ws_bytes,
@@ -1055,6 +1077,10 @@ adahop_status adahop_gemm_mxfp4(const uint8_t *a_codes, const uint8_t *a_scales,
   DeviceInfo di;
   ST_TRY(device_info(&di));
   Ctx cx{reinterpret_cast<cudaStream_t>(stream), static_cast<uint8_t *>(workspace), GemmWs{}, di.num_sms};
+  if (ws_bytes >= adahop_gemm_mxfp4_workspace_size()) {   // room for the stream-K scratch after the header
+    cx.lay.sk = kHeaderBytes;
+    cx.sk = true;
+  }
   return mxf4_gemm(cx, a_codes, a_scales, b_codes, b_scales, P, Q, J, A_o, B_o, r, C, out_dtype);
 }
 

@@ -193,10 +193,118 @@ __device__ __forceinline__ void store_row32(const GemmArgs &g, bool to_partial, 
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Work of one CTA pair of the MXFP4 kernel.  Whole tiles go round robin over the pairs; when the
+// last round would leave pairs idle (sk), the tiles of the last two rounds are cut into their
+// `nsteps` J stages instead, and the stages spread evenly over all pairs (stream-K).  Each pair
+// walks its share of stages from the end: a tile cut between pairs is first worked on by the pairs
+// that hold its first stages (contributors: they leave float32 partial tiles and count their
+// stages on the tile's counter) and last by the pair that holds its final stage (the finisher: it
+// waits for the count, adds the partials, stores C and clears the counter).  A pair holds at most
+// one contributing part (the end of its share, done first) and one finishing part (the start of
+// its share, done last), so no contributor ever waits, and the finisher's wait ends as soon as the
+// other pairs have done their first stream-K part.
+// ---------------------------------------------------------------------------------------------
+enum : int { kItemFull = 0, kItemContrib = 1, kItemFinish = 2 };
+
+struct WorkItem {
+  int64_t tile;        // tile index (n- or m-fastest order, see tile_info)
+  int kb, ke;          // J stages [kb, ke) of the tile
+  int role;
+};
+
+struct WorkSched {
+  int64_t dp_tiles;    // whole tiles, round robin
+  int64_t np;
+  int32_t sk_units;    // stream-K stages over all pairs (the host enables stream-K only below 2^31)
+  int32_t nsteps;
+  // first stream-K stage of pair p
+  __device__ __forceinline__ int32_t lo(int64_t p) const {
+    return static_cast<int32_t>(p * static_cast<int64_t>(sk_units) / np);
+  }
+  // the pair whose share holds stage x: the largest p with lo(p) <= x
+  __device__ __forceinline__ int64_t owner(int32_t x) const {
+    return (static_cast<int64_t>(x + 1) * np + sk_units - 1) / sk_units - 1;
+  }
+};
+
+struct WorkIter {
+  int64_t next_dp;
+  int32_t u_lo, u_hi;
+  int32_t t;           // stream-K tile holding stage u_hi - 1 (kept, not divided out per item)
+};
+
+__device__ __forceinline__ WorkSched make_sched(int64_t num_tiles, int nsteps, int64_t np, bool sk) {
+  WorkSched s;
+  s.np = np;
+  s.nsteps = nsteps;
+  const int64_t rounds = num_tiles / np;
+  s.dp_tiles = !sk ? num_tiles : (rounds >= 1 ? (rounds - 1) * np : 0);
+  s.sk_units = static_cast<int32_t>((num_tiles - s.dp_tiles) * nsteps);
+  return s;
+}
+
+__device__ __forceinline__ WorkIter make_iter(const WorkSched &s, int64_t pair) {
+  WorkIter it{pair, s.lo(pair), s.lo(pair + 1), 0};
+  it.t = it.u_hi > it.u_lo ? (it.u_hi - 1) / s.nsteps : 0;
+  return it;
+}
+
+template <bool SK>
+__device__ __forceinline__ bool next_item(const WorkSched &s, WorkIter &it, WorkItem &w) {
+  if (it.next_dp < s.dp_tiles) {
+    w = WorkItem{it.next_dp, 0, s.nsteps, kItemFull};
+    it.next_dp += s.np;
+    return true;
+  }
+  if constexpr (!SK) return false;
+  if (it.u_hi <= it.u_lo) return false;
+  const int32_t base = it.t * s.nsteps;
+  const int32_t lo = it.u_lo > base ? it.u_lo : base;
+  w.tile = s.dp_tiles + it.t;
+  w.kb = lo - base;
+  w.ke = it.u_hi - base;
+  w.role = (w.kb == 0 && w.ke == s.nsteps) ? kItemFull : (w.ke == s.nsteps ? kItemFinish : kItemContrib);
+  it.u_hi = lo;
+  --it.t;
+  return true;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait for a stream-K counter to reach `target` (false if it ran out or *abort was set).
+__device__ __forceinline__ bool wait_count(const uint32_t *cnt, uint32_t target, const volatile int *abort) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (ld_acquire_u32(cnt) >= target) return true;
+    if ((i & 15u) == 0) {
+      if (abort && *abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// Stream-K exchange: every epilogue warp of a contributing CTA writes the 32 rows x 128 columns of
+// the partial tile it holds (16-byte piece c = 32 half + 8 j + q of row r at float4 c * 128 + r,
+// so a warp's stores cover 512 contiguous bytes) and counts itself on its own counter; the same
+// warp of the finishing CTA waits for the count, then reads the same pieces.  No barrier spans
+// warps, so a warp that gives up a wait never leaves another one waiting on it.
+__device__ __forceinline__ uint32_t *sk_counter(const GemmArgs &g, int64_t sk_tile, uint32_t rank, int ew) {
+  return g.sk_counters + sk_tile * kSkCountersPerTile + rank * kEpiWarps + ew;
+}
+__device__ __forceinline__ float4 *sk_slot(const GemmArgs &g, int64_t pair, uint32_t rank) {
+  return reinterpret_cast<float4 *>(g.sk_partial) + (pair * 2 + rank) * (64 * 128);
+}
+
 // =============================================================================================
 // kind 0: MXFP4 (+ BF16 outlier tail), CTA pairs
 // =============================================================================================
-template <class C>
+template <class C, bool SK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
@@ -214,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t tiles_n = (g.Q + BN - 1) / BN;
   const int64_t num_tiles = tiles_m * tiles_n;
   const bool n_fastest = g.P >= g.Q;                 // stream the larger operand once
+  const WorkSched sched = make_sched(num_tiles, num_k + tail, num_pairs, SK);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -258,15 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const int32_t atoms_per_rowblk = static_cast<int32_t>(g.J >> 7);   // 4-block scale atoms along J
     const int64_t nblocks = (g.Q + 127) >> 7;
-    for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-      const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
+    WorkIter it = make_iter(sched, pair);
+    WorkItem w;
+    while (ok && next_item<SK>(sched, it, w)) {
+      const TileInfo t = tile_info(g, w.tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
       const int32_t my_m0 = static_cast<int32_t>(t.m0 + 128 * rank);
       const int32_t my_n0 = static_cast<int32_t>(t.n0 + 128 * rank);
       const int32_t mb = my_m0 >> 7;
       const int32_t nb0 = static_cast<int32_t>(t.n0 >> 7);
       const int32_t nb1 = (nb0 + 1 < nblocks) ? nb0 + 1 : nb0;   // ragged Q: reuse finite scales
-      const int nsteps = num_k + tail;
-      for (int step = 0; step < nsteps; ++step) {
+      for (int step = w.kb; step < w.ke; ++step) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.empty[stage]), phase ^ 1u, abort_flag, 32))) {
           ok = false;
           break;
@@ -315,14 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       constexpr uint32_t idesc_bf16 = make_idesc_bf16(C::kBM, BN, false, false);
-      for (int64_t tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-        const int nsteps = num_k + tail;
+      WorkIter it = make_iter(sched, pair);
+      WorkItem w;
+      while (ok && next_item<SK>(sched, it, w)) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.acc_empty), acc_phase ^ 1u, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int step = 0; step < nsteps; ++step) {
+        for (int step = w.kb; step < w.ke; ++step) {
           if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag))) {
             ok = false;
             break;
@@ -355,15 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr uint32_t idesc0 = make_idesc_mxf4(C::kBM, BN, 0, 0);
                 constexpr uint32_t idesc2 = make_idesc_mxf4(C::kBM, BN, 2, 2);
                 mma_mxf4_pair(tmem, adesc, bdesc, (kk & 1) ? idesc2 : idesc0, sfa_t + 4 * (kk >> 1),
-                              sfb_t + 8 * (kk >> 1), (step > 0 || kk > 0) ? 1u : 0u);
+                              sfb_t + 8 * (kk >> 1), (step > w.kb || kk > 0) ? 1u : 0u);
               }
             } else {
-              // BF16 outlier tail: four K=16 MMAs over 128-byte rows (never the first step)
+              // BF16 outlier tail: four K=16 MMAs over 128-byte rows (the first of a stream-K part
+              // that starts with a tail stage overwrites the accumulator)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t adesc = make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
                 const uint64_t bdesc = make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
-                mma_bf16_pair(tmem, adesc, bdesc, idesc_bf16, 1u);
+                mma_bf16_pair(tmem, adesc, bdesc, idesc_bf16, (step > w.kb || kk > 0) ? 1u : 0u);
               }
             }
             tc_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);   // frees the stage in both CTAs
@@ -400,8 +512,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t epi_seq = 0;
     uint32_t acc_phase = 0;
     if (lane == 0 && can_store) prefetch_tensormap(&maps.c);
-    for (int64_t tile = pair; tile < num_tiles; tile += num_pairs) {
-      const TileInfo t = tile_info(g, tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
+    const int ew = warp - 2;                           // epilogue warp 0..7
+    const int row_in_cta = 32 * quad + lane;
+    WorkIter it = make_iter(sched, pair);
+    WorkItem w;
+    while (next_item<SK>(sched, it, w)) {
+      const TileInfo t = tile_info(g, w.tile, tiles_m, tiles_n, num_k, n_fastest, C::kBM);
       bool ready = true;
       // polled without back-off: this wait sits on the accumulator hand-off between tiles
       if (lane == 0) ready = mbar_wait(smem_u32(&ctl.acc_full), acc_phase, abort_flag);
@@ -424,6 +540,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty);
       acc_phase ^= 1u;
+
+      if (SK && w.role == kItemContrib) {
+        // this pair's share of the tile's J stages: hand the partial sums to the finisher
+        float4 *slot = sk_slot(g, pair, rank);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            slot[(32 * half + 8 * j + q) * 128 + row_in_cta] =
+                make_float4(__uint_as_float(v[32 * j + 4 * q]), __uint_as_float(v[32 * j + 4 * q + 1]),
+                            __uint_as_float(v[32 * j + 4 * q + 2]), __uint_as_float(v[32 * j + 4 * q + 3]));
+        __threadfence();                             // the partial is visible before the count
+        __syncwarp();
+        if (lane == 0) atomicAdd(sk_counter(g, w.tile - sched.dp_tiles, rank, ew), 1u);
+        continue;
+      }
+      if (SK && w.role == kItemFinish) {
+        // the pairs before this one that hold the tile's earlier stages (each holds one part)
+        const int64_t sk_tile = w.tile - sched.dp_tiles;
+        const uint32_t n_contrib =
+            static_cast<uint32_t>(pair - sched.owner(static_cast<int32_t>(sk_tile) * sched.nsteps));
+        uint32_t *cnt = sk_counter(g, sk_tile, rank, ew);
+        bool got = true;
+        if (lane == 0) got = wait_count(cnt, n_contrib, abort_flag);
+        got = __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
+        if (!got) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            st_cluster_u32(peer_abort, 1u);
+            report_status(g.status, kStatusTimeout);
+          }
+          break;
+        }
+        // add the partials in a fixed order (the nearest pair first): same sums on every run
+        for (uint32_t k = 0; k < n_contrib; ++k) {
+          const float4 *slot = sk_slot(g, pair - 1 - static_cast<int64_t>(k), rank);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 o = __ldcg(slot + (32 * half + 8 * j + q) * 128 + row_in_cta);
+              const int e = 32 * j + 4 * q;
+              v[e] = __float_as_uint(__uint_as_float(v[e]) + o.x);
+              v[e + 1] = __float_as_uint(__uint_as_float(v[e + 1]) + o.y);
+              v[e + 2] = __float_as_uint(__uint_as_float(v[e + 2]) + o.z);
+              v[e + 3] = __float_as_uint(__uint_as_float(v[e + 3]) + o.w);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) *cnt = 0u;                    // read by this warp only: clear it for the next launch
+      }
 
       // Stores through shared memory: each 32-row x 32-byte box (16 bf16 or 8 fp32 columns) is
       // written by the warp into its staging buffer, lane i filling row i with the 32-byte swizzle
@@ -956,7 +1123,8 @@ int pair_capacity(int num_sms) {
   const cudaLaunchConfig_t cfg =
       pair_launch_config(attr, static_cast<unsigned>(num_sms & ~1), C::kSmemBytes + 1024, 0);
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf4_pair_kernel<C>, &cfg) != cudaSuccess || clusters <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf4_pair_kernel<C, false>, &cfg) != cudaSuccess ||
+      clusters <= 0) {
     (void)cudaGetLastError();
     clusters = num_sms / 2;
   }
@@ -965,17 +1133,36 @@ int pair_capacity(int num_sms) {
 }
 
 template <class C>
-cudaError_t launch_mxf4_cfg(const GemmArgs &g, const GemmMaps &maps, int num_sms, cudaStream_t s) {
+cudaError_t launch_mxf4_cfg(const GemmArgs &g0, const GemmMaps &maps, int num_sms, cudaStream_t s) {
   const size_t smem = C::kSmemBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  GemmArgs g = g0;
   const int64_t tiles = ((g.P + C::kBM - 1) / C::kBM) * ((g.Q + BN - 1) / BN);
   const int64_t cap = pair_capacity<C>(num_sms);
-  const unsigned pairs = static_cast<unsigned>(tiles < cap ? tiles : cap);
+  int64_t pairs = tiles < cap ? tiles : cap;
+  // Stream-K where it measured faster: at least two whole rounds of tiles, a last round that
+  // would leave over 3% of the pairs idle, and a long J (the wgrad shapes with few tiles).  With
+  // fewer rounds, or a short J, splitting tiles across pairs loses more to operand reuse in L2
+  // (pairs no longer stream the same J slices of shared operand rows together) than it gains.
+  g.sk = 0;
+  if (g.sk_partial && g.sk_counters && cap <= g.sk_max_pairs && g.J >= 16384) {
+    const int64_t rounds = (tiles + cap - 1) / cap;
+    const int64_t dp = tiles / cap >= 1 ? (tiles / cap - 1) * cap : 0;
+    const int64_t nsteps = (g.J + C::kBK - 1) / C::kBK + g.tail_stages;
+    const int64_t units = (tiles - dp) * nsteps;
+    const bool short_round = tiles < 97 * rounds * cap / 100;
+    // every pair needs at least one stage (the finisher counts the pairs before it as contributors)
+    if (tiles >= 2 * cap && short_round && tiles - dp <= kSkMaxTiles && units >= cap &&
+        units < (int64_t(1) << 31)) {
+      g.sk = 1;
+      pairs = cap;
+    }
+  }
+  auto *kernel = g.sk ? gemm_mxf4_pair_kernel<C, true> : gemm_mxf4_pair_kernel<C, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = pair_launch_config(attr, 2 * pairs, smem, s);
-  e = cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<C>, maps, g);
+  const cudaLaunchConfig_t cfg = pair_launch_config(attr, static_cast<unsigned>(2 * pairs), smem, s);
+  e = cudaLaunchKernelEx(&cfg, kernel, maps, g);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

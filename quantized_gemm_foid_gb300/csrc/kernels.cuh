@@ -89,7 +89,20 @@ struct GemmArgs {
   const int32_t *scatter_idx;
   int scatter_axis;
   int64_t c_rows, c_cols;
+  // kind 0: stream-K for the tiles a whole round cannot fill (sk != 0, set by launch_gemm when the
+  // caller provides both buffers): float32 partial tiles of the contributing pairs (sk_partial,
+  // kSkPartialBytesPerPair per pair, at most sk_max_pairs pairs) and kSkCountersPerTile counters per
+  // stream-K tile (sk_counters, zero when the launch starts; the launch leaves them zero).
+  int sk;
+  float *sk_partial;
+  uint32_t *sk_counters;
+  int sk_max_pairs;
 };
+// Stream-K scratch of the fused MXFP4 GEMM: one 256 x 256 float32 partial tile per CTA pair, and
+// 16 counters per stream-K tile (2 CTAs x 8 epilogue warps), at most kSkMaxTiles tiles.
+constexpr size_t kSkPartialBytesPerPair = 256 * 256 * 4;
+constexpr int kSkMaxTiles = 160;
+constexpr int kSkCountersPerTile = 16;
 // MXFP4: a / b are the E2M1 codes (128-byte rows, 128 rows per box), sfa / sfb the tensor-core
 // scale atoms viewed as rows of 128 uint32 (one 512-byte atom per row, two atoms per box), ao / bo
 // the BF16 outlier slices, c the output C (MXFP4 only: 32-row boxes of 32 bytes, 32-byte swizzle,

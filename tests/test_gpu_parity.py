@@ -243,7 +243,7 @@ def test_calibration_classes(q):
         dX, dW, dG = X.cuda(), W.cuda(), GY.cuda()
         M, K = X.shape
         N = W.shape[0]
-        ws = q.new_workspace(4 * (max(M, N) + max(N, K)) + 4096)
+        ws = q.new_workspace(16384 + 4 * (max(M, N) + max(N, K)) + 512)   # zeroed header + statistics
         plan = q.adahop_calibrate(dX, dW, dG, ws)
         assert (plan.x, plan.w, plan.gy) == (want["patterns"]["X"], want["patterns"]["W"],
                                              want["patterns"]["GY"])
@@ -261,7 +261,10 @@ def _rel(got, ref):
                                    (256, 384, 2304), (384, 256, 4096)])
 @pytest.mark.parametrize("r", [0, 16, 64, 128])
 @pytest.mark.parametrize("out", ["fp32", "bf16"])
-def test_gemm_mxfp4_against_oracle(q, P, Q, J, r, out):
+@pytest.mark.parametrize("stream_k", [False, True])
+def test_gemm_mxfp4_against_oracle(q, P, Q, J, r, out, stream_k):
+    """With a 4 KB workspace and with the one that allows stream-K (these shapes have too few tiles
+    for it, so both run whole tiles: the larger workspace changes nothing here)."""
     A = _bits((P, J), 31, axis="col", count=4, scale=30.0)
     Bt = _bits((Q, J), 32, std=0.02)
     ac, asf = O.quantize_operand(A, True)
@@ -274,14 +277,53 @@ def test_gemm_mxfp4_against_oracle(q, P, Q, J, r, out):
         ref = ref + O.bf16_to_f32(Ao_bits).astype(np.float64) @ O.bf16_to_f32(Bo_bits).astype(np.float64).T
         Ao, Bo = dev_bf16_from_bits(Ao_bits), dev_bf16_from_bits(Bo_bits)
     C = torch.zeros((P, Q), dtype=torch.float32 if out == "fp32" else torch.bfloat16, device="cuda")
-    ws = q.new_workspace(4096)
-    q.adahop_gemm_mxfp4(to_dev(ac), to_dev(to_tiled(asf)), to_dev(bc), to_dev(to_tiled(bsf)), P, Q, J, Ao, Bo, r,
-                        C, ws)
+    ws = q.new_workspace(q.adahop_gemm_mxfp4_workspace_size() if stream_k else 4096)
+    args = (to_dev(ac), to_dev(to_tiled(asf)), to_dev(bc), to_dev(to_tiled(bsf)), P, Q, J, Ao, Bo, r)
+    q.adahop_gemm_mxfp4(*args, C, ws)
     assert q.adahop_get_device_status(ws) == 0
     got = C.float().cpu().numpy().astype(np.float64)
     assert _rel(got, ref) <= (TOL_FP32 if out == "fp32" else TOL_BF16)
     if out == "fp32":
         assert _rel(got, ref) <= 1e-5          # float32 accumulation of exact products
+    if stream_k:
+        C2 = torch.full_like(C, 7.0)
+        q.adahop_gemm_mxfp4(*args, C2, ws)
+        assert q.adahop_get_device_status(ws) == 0
+        assert torch.equal(C, C2)
+
+
+# at least two whole rounds of 256 x 256 tiles over the CTA pairs, a short last round and a long J:
+# the shapes the fused GEMM balances with stream-K (160 tiles; 256 tiles like the q / o wgrad)
+@pytest.mark.parametrize("P,Q,J,r", [(4096, 2560, 16384, 0), (4096, 2560, 16384, 64), (4096, 4096, 32768, 64)])
+def test_gemm_mxfp4_stream_k_matches_whole_tiles(q, P, Q, J, r):
+    """Stream-K (the workspace the entry point asks for) against whole tiles (a 4 KB workspace,
+    itself checked against the oracle above): equal to float32 rounding of the reordered sums,
+    bit-identical on a second call, and the counters left at zero."""
+    A = normal_bf16(P, J, 1.0, 41, device="cuda")
+    B = normal_bf16(Q, J, 0.02, 42, device="cuda")
+    ac = torch.empty(P * J // 2, dtype=torch.uint8, device="cuda")
+    asf = torch.empty(P * J // 32, dtype=torch.uint8, device="cuda")
+    bc = torch.empty(Q * J // 2, dtype=torch.uint8, device="cuda")
+    bsf = torch.empty(Q * J // 32, dtype=torch.uint8, device="cuda")
+    q.adahop_quantize_mxfp4(A, 1, 1, None, None, ac, asf, 1)
+    q.adahop_quantize_mxfp4(B, 1, 1, None, None, bc, bsf, 1)
+    del A, B
+    Ao = normal_bf16(P, r, 5.0, 43, device="cuda") if r else None
+    Bo = normal_bf16(Q, r, 0.02, 44, device="cuda") if r else None
+    Cw = torch.empty((P, Q), dtype=torch.float32, device="cuda")
+    Cs = torch.empty((P, Q), dtype=torch.float32, device="cuda")
+    ws_w = q.new_workspace(4096)
+    ws_s = q.new_workspace(q.adahop_gemm_mxfp4_workspace_size())
+    q.adahop_gemm_mxfp4(ac, asf, bc, bsf, P, Q, J, Ao, Bo, r, Cw, ws_w)
+    q.adahop_gemm_mxfp4(ac, asf, bc, bsf, P, Q, J, Ao, Bo, r, Cs, ws_s)
+    assert q.adahop_get_device_status(ws_w) == 0 and q.adahop_get_device_status(ws_s) == 0
+    diff = (Cs.double() - Cw.double()).norm() / Cw.double().norm()
+    assert float(diff) <= 1e-6
+    Cs2 = torch.full_like(Cs, 3.0)
+    q.adahop_gemm_mxfp4(ac, asf, bc, bsf, P, Q, J, Ao, Bo, r, Cs2, ws_s)
+    assert q.adahop_get_device_status(ws_s) == 0
+    assert torch.equal(Cs, Cs2)
+    assert int(ws_s[:16384].count_nonzero()) == 0
 
 
 @pytest.mark.parametrize("a_kmajor,b_kmajor", [(1, 1), (1, 0), (0, 0), (0, 1)])
