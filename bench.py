@@ -49,8 +49,8 @@ MX_BYTES_PER_ELEM = 0.5 + 1 / 32             # one E2M1 code + its share of an E
 # captures (dram__bytes_read.sum + dram__bytes_write.sum).  It describes the kernel source it was
 # taken on (sha256 over the files below); for any other source the bench reports traffic as null.
 GEMM_SOURCES = ("quantized_gemm_foid_gb300/csrc/gemm.cu", "quantized_gemm_foid_gb300/csrc/common.cuh")
-GEMM_TRAFFIC = {"source_sha256": "5b95a0210224c4d2da5a2a31e4348efde00a426648e8a27dc29305432bfbbadb",
-                "bytes_per_launch": 538105209}
+GEMM_TRAFFIC = {"source_sha256": "29b904ddaa8ddd5a632b03b06f7849e6fb8e651e653dc7514cb0f37033eb7831",
+                "bytes_per_launch": 538339023}
 
 
 # ------------------------------------------------------------------------------------ helpers
@@ -141,11 +141,22 @@ def gemm_traffic():
     return None
 
 
-def cuda_time_ms(fn, reps: int, stream=None) -> float:
-    """Average device time of fn() over reps, CUDA events on the launching (current) stream."""
+def hold_device(reps: int, us_per_rep: float = 100.0) -> None:
+    """Queues a spin of about reps x us_per_rep microseconds on the current stream, so that the
+    host has enqueued the launches that follow before the device reaches them: the events around
+    them then time the kernels, not the host's per-call work (argument checks, tensor-map
+    encoding) in front of the first one."""
+    torch.cuda._sleep(int(reps * us_per_rep * 2000))     # cycles at ~2 GHz
+
+
+def cuda_time_ms(fn, reps: int, stream=None, hold: bool = False) -> float:
+    """Average device time of fn() over reps, CUDA events on the launching (current) stream;
+    hold: the device waits until the host has queued every rep (kernel timing)."""
     s = stream or torch.cuda.current_stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    if hold:
+        hold_device(reps)
     start.record(s)
     for _ in range(reps):
         fn()
@@ -373,13 +384,15 @@ class Bench:
                     Bo = torch.randn((Q, r), device=self.device).to(torch.bfloat16)
                 out = c.Y if gemm == "fwd" else (c.dX if gemm == "dgrad" else c.dW)
                 ms = cuda_time_ms(lambda: q.adahop_gemm_mxfp4(ac, asf, bc, bsf, P, Q, J, Ao, Bo, r, out, self.ws),
-                                  reps)
+                                  reps, hold=True)
                 f = 2 * P * Q * J + 2 * P * Q * r
                 tot_flops += f
                 tot_s += ms / 1e3
-                tot_bytes += (P + Q) * J * MX_BYTES_PER_ELEM + 2 * (P + Q) * r + 2 * P * Q
+                nbytes = (P + Q) * J * MX_BYTES_PER_ELEM + 2 * (P + Q) * r + 2 * P * Q
+                tot_bytes += nbytes
                 per.append({"linear": c.name, "gemm": gemm, "P": P, "Q": Q, "J": J, "r": r,
-                            "ms": round(ms, 4), "tflops": round(f / ms / 1e9, 1)})
+                            "ms": round(ms, 4), "tflops": round(f / ms / 1e9, 1),
+                            "gbs": round(nbytes / ms / 1e6, 1)})
                 del ac, asf, bc, bsf, Ao, Bo
         return tot_flops, tot_s, per, tot_bytes
 
@@ -393,7 +406,8 @@ class Bench:
             n = c.M * c.N
             codes = torch.empty(n // 2, dtype=torch.uint8, device=self.device)
             sf = torch.empty(n // 32, dtype=torch.uint8, device=self.device)
-            ms = cuda_time_ms(lambda: q.adahop_quantize_mxfp4(c.GY, axis, 1, None, None, codes, sf, 1), reps)
+            ms = cuda_time_ms(lambda: q.adahop_quantize_mxfp4(c.GY, axis, 1, None, None, codes, sf, 1), reps,
+                              hold=True)
             out[name] = {"ms": round(ms, 4), "gbs": round(n * QUANT_BYTES_PER_ELEM / ms / 1e6, 1),
                          "shape": [c.M, c.N]}
         # both orientations from one read (the step's G_Y / X / W pass): 2 + 2 x 0.53 B per element
@@ -402,7 +416,8 @@ class Bench:
         sr = torch.empty(n // 32, dtype=torch.uint8, device=self.device)
         cc = torch.empty(n // 2, dtype=torch.uint8, device=self.device)
         sc = torch.empty(n // 32, dtype=torch.uint8, device=self.device)
-        ms = cuda_time_ms(lambda: q.adahop_quantize_mxfp4_dual(c.GY, 1, None, None, cr, sr, cc, sc, 1), reps)
+        ms = cuda_time_ms(lambda: q.adahop_quantize_mxfp4_dual(c.GY, 1, None, None, cr, sr, cc, sc, 1), reps,
+                          hold=True)
         out["dual"] = {"ms": round(ms, 4), "gbs": round(n * (2 + 2 * MX_BYTES_PER_ELEM) / ms / 1e6, 1),
                        "shape": [c.M, c.N]}
         return out
@@ -572,9 +587,18 @@ def copy_probe(q, device, nbytes: int = 2 << 30, reps: int = 5) -> float:
     src = torch.empty(nbytes, dtype=torch.uint8, device=device)
     dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
     q.adahop_probe_copy(src, dst)
-    best = min(cuda_time_ms(lambda: q.adahop_probe_copy(src, dst), 1) for _ in range(reps))
+    best = min(cuda_time_ms(lambda: q.adahop_probe_copy(src, dst), 1, hold=True) for _ in range(reps))
     del src, dst
     return round(2 * nbytes / best / 1e6, 1)
+
+
+def fill_probe(q, device, nbytes: int = 4 << 30, reps: int = 5) -> float:
+    """HBM write-only GB/s of the library's streaming fill (K8), best of `reps` 4 GiB fills."""
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    q.adahop_probe_copy(None, dst)
+    best = min(cuda_time_ms(lambda: q.adahop_probe_copy(None, dst), 1, hold=True) for _ in range(reps))
+    del dst
+    return round(nbytes / best / 1e6, 1)
 
 
 def roofline_fields(achieved: float, peaks: dict, peak_kind: str, pipe: dict, gemm_mhz) -> dict:
@@ -606,7 +630,7 @@ def peaks_report(q, device) -> dict:
     # a 128-wide MMA takes half as long: can one lane still issue four MMAs and their copies?
     for kind, sf in ((0, 0), (1, 0), (1, 1)):
         rates[f"{q.MMA_KIND_NAMES[kind]}{' +sf' if sf else ''} N=128"] = pipe_probe(q, kind, sf, n=128)
-    return {"mma": rates, "copy_gbs": copy_probe(q, device)}
+    return {"mma": rates, "copy_gbs": copy_probe(q, device), "fill_gbs": fill_probe(q, device)}
 
 
 # ------------------------------------------------------------------------------------ CPU oracle
@@ -898,26 +922,44 @@ def sweep(q, device, args):
     print(json.dumps({"sweep": "llama3.1-8b down projection, Fwd", "K": K, "N": N, "points": points}))
 
 
-def outlier_splits_sweep(q, device):
-    """Split-K of the outer-OE outlier GEMM on the step's shapes, O = G_Y[idx, :] (64 x J) times W
-    (J x Q, read MN-major) into float32 partials: microseconds per launch (CUDA events, 20
-    launches) for each number of splits.  Prints one JSON object."""
+def outlier_times(q, device, reps: int = 20) -> dict:
+    """The outer-OE outlier GEMM with its scatter-add fused (dX[idx, :] += G_Y[idx, :] . W) on the
+    step's four dgrad shapes: microseconds per launch, CUDA events around each launch alone, with
+    a 256 MB write between launches so that W (up to 117 MB) is read from DRAM as in the step
+    (every launch queued before the device reaches the first).
+    GB/s counts the algorithmic bytes: W once, the r extracted rows, the r rows of dX read and
+    written."""
     from synthetic import normal_bf16
-    ws = q.new_workspace(4096, device=device)
+    r, M = 64, 32768
+    ws = q.new_workspace(256, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     out = {}
-    for name, P, Q, J in (("gate", 64, 4096, 14336), ("down", 64, 14336, 4096), ("q", 64, 4096, 4096),
-                          ("k", 64, 4096, 1024)):
-        A = normal_bf16(P, J, 1.0, 1, device=device)
-        B = normal_bf16(J, Q, 0.02, 2, device=device)
-        res = {}
-        for S in (1, 2, 4, 6, 8, 9, 12, 16):
-            part = torch.empty((S, P, Q), dtype=torch.float32, device=device)
-            res[S] = round(1e3 * cuda_time_ms(
-                lambda: q.adahop_gemm_bf16(A, 1, B, 0, P, Q, J, None, ws, splits=S, c_partial=part), 20), 2)
-        out[name] = res
+    for name, J, Q in (("gate/up", 14336, 4096), ("down", 4096, 14336), ("q/o", 4096, 4096),
+                       ("k/v", 1024, 4096)):
+        A = normal_bf16(r, J, 1.0, 1, device=device)
+        B = normal_bf16(J, Q, 0.02, 2, device=device)          # W as dgrad reads it: J x Q, MN-major
+        C = torch.zeros((M, Q), dtype=torch.bfloat16, device=device)
+        idx = torch.randperm(M, device=device)[:r].sort().values.to(torch.int32)
+        fn = lambda: q.adahop_gemm_bf16_scatter_add(A, 1, B, 0, r, Q, J, C, idx, r, 0, ws)
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        hold_device(reps, 200.0)
+        for s, e in ev:
+            flush.fill_(1)
+            s.record()
+            fn()
+            e.record()
+        torch.cuda.synchronize()
+        us = 1e3 * sum(s.elapsed_time(e) for s, e in ev) / reps
+        nbytes = 2 * (J * Q + r * J + 2 * r * Q)
+        out[name] = {"P": r, "Q": Q, "J": J, "us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1),
+                     "algorithmic_bytes": nbytes}
+        del A, B, C
     if q.adahop_get_device_status(ws) != 0:
-        raise SystemExit("device status after the sweep")
-    print(json.dumps({"outlier_gemm_us_by_splits": out}), flush=True)
+        raise SystemExit("device status after the outlier GEMMs")
+    return out
 
 
 def batch_sweep(q, device, args):
@@ -1066,23 +1108,35 @@ def profile(q, device, args):
         torch.cuda.synchronize()
         print("profiled 3 scatter-add launches")
         return
-    if args.profile in ("bf16", "outlier"):
+    if args.profile == "bf16":                          # BF16 strategy / baseline: q projection fwd
         ws = q.new_workspace(4096, device=device)
-        if args.profile == "bf16":                      # BF16 strategy / baseline: q projection fwd
-            P, Q, J, S = 32768, 4096, 4096, 1
-        else:                                           # outer-OE outlier GEMM: 64 rows x W (gate dgrad)
-            P, Q, J, S = 64, 4096, 14336, 8
+        P, Q, J = 32768, 4096, 4096
         A = normal_bf16(P, J, 1.0, 1, device=device)
-        # fwd: B^T = W stored Q x J (K-major); outlier GEMM: B = W stored J x Q (MN-major), as dgrad reads it
-        b_kmajor = 1 if args.profile == "bf16" else 0
-        B = normal_bf16(Q, J, 0.02, 2, device=device) if b_kmajor else normal_bf16(J, Q, 0.02, 2, device=device)
-        C = torch.empty((P, Q), dtype=torch.bfloat16, device=device) if S == 1 else None
-        part = torch.empty((S, P, Q), dtype=torch.float32, device=device) if S > 1 else None
+        B = normal_bf16(Q, J, 0.02, 2, device=device)   # B^T = W stored Q x J (K-major)
+        C = torch.empty((P, Q), dtype=torch.bfloat16, device=device)
         for _ in range(3):
-            q.adahop_gemm_bf16(A, 1, B, b_kmajor, P, Q, J, C, ws, splits=S, c_partial=part)
+            q.adahop_gemm_bf16(A, 1, B, 1, P, Q, J, C, ws)
         torch.cuda.synchronize()
         assert q.adahop_get_device_status(ws) == 0
-        print(f"profiled 3 BF16 GEMM launches ({P} x {Q} x {J}, splits {S})")
+        print(f"profiled 3 BF16 GEMM launches ({P} x {Q} x {J})")
+        return
+    if args.profile == "outlier":
+        # the gate dgrad's outer-OE outlier GEMM with the scatter-add fused: dX[idx, :] +=
+        # G_Y[idx, :] (64 x 14336) . W (14336 x 4096, read MN-major); a 256 MB write before each of
+        # the three launches so that W comes from DRAM
+        r, M, J, Q = 64, 32768, 14336, 4096
+        ws = q.new_workspace(256, device=device)
+        A = normal_bf16(r, J, 1.0, 1, device=device)
+        B = normal_bf16(J, Q, 0.02, 2, device=device)
+        C = torch.zeros((M, Q), dtype=torch.bfloat16, device=device)
+        idx = torch.randperm(M, device=device)[:r].sort().values.to(torch.int32)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        for _ in range(3):
+            flush.fill_(1)
+            q.adahop_gemm_bf16_scatter_add(A, 1, B, 0, r, Q, J, C, idx, r, 0, ws)
+        torch.cuda.synchronize()
+        assert q.adahop_get_device_status(ws) == 0
+        print(f"profiled 3 fused outlier GEMM + scatter-add launches ({r} x {Q} x {J})")
         return
     if args.profile == "quant1":
         M, N = 32768, 14336
@@ -1106,6 +1160,29 @@ def profile(q, device, args):
             q.adahop_quantize_mxfp4_dual(G, 1, None, None, cr, sr, cc, sc, 1)
         torch.cuda.synchronize()
         print("profiled 3 dual-orientation quantiser launches")
+        return
+    if args.profile == "gemm_sk":
+        # the q wgrad shape (P = Q = 4096, J = 32768, inner-OE tail r = 64), which the fused GEMM
+        # runs with stream-K: three launches
+        P, Q, J, r = 4096, 4096, 32768, 64
+        A = normal_bf16(P, J, 1e-3, 1, device=device)
+        B = normal_bf16(Q, J, 1.0, 2, device=device)
+        ac = torch.empty(P * J // 2, dtype=torch.uint8, device=device)
+        asf = torch.empty(P * J // 32, dtype=torch.uint8, device=device)
+        bc = torch.empty(Q * J // 2, dtype=torch.uint8, device=device)
+        bsf = torch.empty(Q * J // 32, dtype=torch.uint8, device=device)
+        q.adahop_quantize_mxfp4(A, 1, 1, None, None, ac, asf, 1)
+        q.adahop_quantize_mxfp4(B, 1, 1, None, None, bc, bsf, 1)
+        del A, B
+        Ao = torch.randn((P, r), device=device).to(torch.bfloat16)
+        Bo = torch.randn((Q, r), device=device).to(torch.bfloat16)
+        C = torch.empty((P, Q), dtype=torch.bfloat16, device=device)
+        ws = q.new_workspace(q.adahop_gemm_mxfp4_workspace_size(), device=device)
+        for _ in range(3):
+            q.adahop_gemm_mxfp4(ac, asf, bc, bsf, P, Q, J, Ao, Bo, r, C, ws)
+        torch.cuda.synchronize()
+        assert q.adahop_get_device_status(ws) == 0
+        print("profiled 3 stream-K fused MXFP4 GEMM launches (4096 x 4096 x 32768, r = 64)")
         return
     P, Q, J = 32768, 4096, 14336
     A = normal_bf16(P, J, 1e-3, 1, device=device)
@@ -1137,23 +1214,25 @@ def main():
     ap.add_argument("--batch-sweep", action="store_true",
                     help="throughput against batch size (seq_len 4096, batch 1..16), AdaHOP and BF16 plans; "
                          "prints one JSON object")
-    ap.add_argument("--outlier-splits", action="store_true",
-                    help="split-K sweep of the outer-OE outlier GEMM on the step's shapes; prints one JSON object")
+    ap.add_argument("--outlier", action="store_true",
+                    help="the fused outer-OE outlier GEMM + scatter-add on the step's four dgrad shapes, "
+                         "L2 flushed between launches; prints one JSON object")
     ap.add_argument("--quality", action="store_true",
                     help="relative MSE of the Table 3 plans on the 8B gate projection; prints one JSON object")
-    ap.add_argument("--profile", choices=["step", "bwd", "gemm", "gemms", "quant", "quant1", "foid", "scatter",
-                                          "bf16", "outlier"],
+    ap.add_argument("--profile", choices=["step", "bwd", "gemm", "gemm_sk", "gemms", "quant", "quant1", "foid",
+                                          "scatter", "bf16", "outlier"],
                     default=None,
                     help="for ncu only (prints no bench line): 'step' = warm-up steps then one step "
                          "of the workload; 'bwd' = two fwd + bwd passes of the gate projection alone; "
                          "'gemm' = three launches of the fused MXFP4 GEMM on the "
-                         "dgrad shape P=32768, Q=4096, J=14336; 'gemms' = two launches of it on each of the "
+                         "dgrad shape P=32768, Q=4096, J=14336; 'gemm_sk' = three on the q wgrad shape "
+                         "(4096 x 4096 x 32768, stream-K); 'gemms' = two launches of it on each of the "
                          "step's 21 shapes, one shape's operands at a time; 'quant' = three launches of the "
                          "dual-orientation quantiser on the 32768 x 14336 G_Y; 'quant1' = three rows- "
                          "and three cols-orientation launches on it; 'foid' = three row FOID calls on it "
                          "(r = 64); 'scatter' = three scatter-adds of 64 rows into 32768 x 4096; 'bf16' = "
-                         "three BF16 GEMMs 32768 x 4096 x 4096; 'outlier' = three split-K BF16 GEMMs "
-                         "64 x 4096 x 14336 (8 splits)")
+                         "three BF16 GEMMs 32768 x 4096 x 4096; 'outlier' = three fused outlier GEMM + "
+                         "scatter-add launches of the gate dgrad (64 x 4096 x 14336)")
     ap.add_argument("--peaks", action="store_true",
                     help="K8 probes only: every MMA kind's rate and the streaming copy; prints one JSON object")
     ap.add_argument("--cpu-worker", type=int, default=None, help=argparse.SUPPRESS)
@@ -1186,8 +1265,8 @@ def main():
     if args.batch_sweep:
         batch_sweep(q, device, args)
         return
-    if args.outlier_splits:
-        outlier_splits_sweep(q, device)
+    if args.outlier:
+        print(json.dumps({"outlier_gemm_scatter_add": outlier_times(q, device)}), flush=True)
         return
 
     peaks, peak_kind = load_peaks()
@@ -1214,6 +1293,7 @@ def main():
     gclk = gemm_clocks.stop()
     pipe = pipe_probe(q)
     copy_gbs = copy_probe(q, device)
+    fill_gbs = fill_probe(q, device)
     prep = b.prep_bandwidth()
     variants = b.variants()
     g_ms = b.graph_ms()
@@ -1224,9 +1304,9 @@ def main():
 
     # freshly pinned host buffers run slow for their first few steps (a training loop refills the
     # same pinned buffers every step), so five untimed steps come first; the host path is shared
-    # with other jobs and its speed comes and goes over seconds, so three trials are timed and the
+    # with other jobs and its speed comes and goes over seconds, so five trials are timed and the
     # median one is reported, every trial listed
-    e2e_trials, h2d, d2h, copy_trials = b.e2e(steps=5, warmup=5, trials=3)
+    e2e_trials, h2d, d2h, copy_trials = b.e2e(steps=5, warmup=5, trials=5)
     # whole job, like `value`: every rank's work over the slowest rank's (median-trial) time
     e2e_ms = max_over_ranks(world, sorted(e2e_trials)[len(e2e_trials) // 2])
     link = host_link_gbs(device)
@@ -1243,7 +1323,7 @@ def main():
                          traffic=gemm_traffic(), traffic_unit="bytes per launch (DRAM, ncu)",
                          algorithmic_bytes=gbytes / max(1, len(per_gemm)), launches=len(per_gemm)),
         "prep": {"kernel": "IHT + MXFP4 quantiser", "bound": "hbm", "peak_gbs": hbm, "peak_source": peak_kind,
-                 "copy_probe_gbs": copy_gbs, "nominal_gbs": NOMINAL["hbm_gbs"],
+                 "copy_probe_gbs": copy_gbs, "fill_probe_gbs": fill_gbs, "nominal_gbs": NOMINAL["hbm_gbs"],
                  **{k: dict(v, frac=round(v["gbs"] / hbm, 3), frac_copy_probe=round(v["gbs"] / copy_gbs, 3),
                             frac_nominal=round(v["gbs"] / NOMINAL["hbm_gbs"], 3)) for k, v in prep.items()}},
         "variants": variants,

@@ -348,7 +348,9 @@ adahop_status adahop_probe_mma_rate(int kind, int sf_copies, int n, int64_t iter
 /* Streaming copy probe: dst[0:bytes] = src[0:bytes] with 16-byte loads and stores (streaming
  * cache hints), grid sized to the SM count.  bytes a multiple of 16, pointers 16-byte aligned,
  * buffers must not overlap.  Time it on `stream` (2 x bytes of DRAM traffic per call).
- * Asynchronous. */
+ * src NULL: write-only stream instead, every 16-bit half-word of dst[0:bytes] set to 0x3F80
+ * (bytes of DRAM writes per call; the denominator for store-bound kernels).  dst NULL:
+ * ADAHOP_ERR_INVALID_ARG.  Asynchronous. */
 adahop_status adahop_probe_copy(const void *src, void *dst, size_t bytes, adahop_stream_t stream);
 
 #ifdef __cplusplus

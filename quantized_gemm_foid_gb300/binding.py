@@ -301,9 +301,13 @@ def adahop_probe_mma_rate(kind: int, sf_copies: int, iters: int, out, ws, stream
 
 
 def adahop_probe_copy(src, dst, stream=None) -> None:
-    _cuda(src, "src")
+    """src None: the write-only fill of all of dst."""
     _cuda(dst, "dst")
-    nbytes = src.numel() * src.element_size()
-    if dst.numel() * dst.element_size() < nbytes:
-        raise ValueError("dst is smaller than src")
+    if src is None:
+        nbytes = dst.numel() * dst.element_size()
+    else:
+        _cuda(src, "src")
+        nbytes = src.numel() * src.element_size()
+        if dst.numel() * dst.element_size() < nbytes:
+            raise ValueError("dst is smaller than src")
     _check(LIB.adahop_probe_copy(_p(src), _p(dst), nbytes, _stream(stream)), "adahop_probe_copy")

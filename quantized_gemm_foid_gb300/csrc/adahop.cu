@@ -954,9 +954,9 @@ adahop_status adahop_probe_mma_rate(int kind, int sf_copies, int n, int64_t iter
 }
 
 adahop_status adahop_probe_copy(const void *src, void *dst, size_t bytes, adahop_stream_t stream) {
-  if (!src || !dst) return ADAHOP_ERR_INVALID_ARG;
+  if (!dst) return ADAHOP_ERR_INVALID_ARG;
   if (bytes % 16) return ADAHOP_ERR_SHAPE;
-  if (!aligned(src, 16) || !aligned(dst, 16)) return ADAHOP_ERR_ALIGN;
+  if ((src && !aligned(src, 16)) || !aligned(dst, 16)) return ADAHOP_ERR_ALIGN;
   DeviceInfo di;
   ST_TRY(device_info(&di));
   CUDA_TRY(launch_copy_probe(src, dst, bytes, di.num_sms, reinterpret_cast<cudaStream_t>(stream)), "copy probe launch");

@@ -10,7 +10,8 @@ namespace adahop {
 // Byte offset of scale factor (line, 32-block blk) in the tensor-core scale layout: atoms of
 // 128 lines x 4 blocks (512 bytes), atom (line/128, blk/4) at ((line/128)*(J/128) + blk/4)*512,
 // and inside the atom byte (line%32)*16 + ((line%128)/32)*4 + blk%4.
-__host__ __device__ __forceinline__ int64_t tiled_sf_offset(int64_t line, int64_t blk, int64_t J) {
+template <class I>
+__host__ __device__ __forceinline__ I tiled_sf_offset(I line, I blk, I J) {
   return ((line >> 7) * (J >> 7) + (blk >> 2)) * 512 + (line & 31) * 16 + ((line >> 5) & 3) * 4 +
          (blk & 3);
 }

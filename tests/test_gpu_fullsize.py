@@ -82,3 +82,37 @@ def test_quantize_dual_full_size_sampled_lines(q, gate_gy, foid_rows):
     got_c = cc.view(N, M // 2)[torch.from_numpy(cols).cuda()].cpu().numpy()
     assert np.array_equal(got_c, wc)
     assert np.array_equal(from_tiled(to_host_u8(sc), cols, M), ws)
+
+
+def test_quantize_dual_64bit_offsets():
+    """A tensor of 2^31 elements (32768 x 65536, 4 GiB of bf16), which takes the dual quantiser's
+    64-bit-offset instantiation (below 2^31 elements it computes offsets in 32 bits): both
+    orientations equal the single-orientation kernels bit for bit, and sampled lines near the
+    ends of the tensor, where the offsets pass 2^31, equal the oracle's.  About 17 GB on the
+    device at the peak (the float32 draw of the tensor)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_gemm_foid_gb300 as q
+    from synthetic import normal_bf16
+    M, N = 32768, 65536
+    n = M * N
+    assert n == 1 << 31
+    T = normal_bf16(M, N, 1.0, 11, device="cuda")
+    bufs = [torch.empty(k, dtype=torch.uint8, device="cuda") for k in (n // 2, n // 32, n // 2, n // 32)]
+    cr, sr, cc, sc = bufs
+    q.adahop_quantize_mxfp4_dual(T, 1, None, None, cr, sr, cc, sc, 1)
+    for axis, codes, scales in ((1, cr, sr), (0, cc, sc)):
+        c1 = torch.empty_like(codes)
+        s1 = torch.empty_like(scales)
+        q.adahop_quantize_mxfp4(T, axis, 1, None, None, c1, s1, 1)
+        torch.cuda.synchronize()
+        assert torch.equal(c1, codes) and torch.equal(s1, scales)
+        del c1, s1
+    rows = np.array([0, 1, M // 2, M - 65, M - 2, M - 1])
+    wc, ws = O.quantize_operand(bf16_bits(T[torch.from_numpy(rows).cuda()]), True)
+    assert np.array_equal(cr.view(M, N // 2)[torch.from_numpy(rows).cuda()].cpu().numpy(), wc)
+    assert np.array_equal(from_tiled(to_host_u8(sr), rows, N), ws)
+    cols = np.array([0, 127, N // 2, N - 129, N - 1])
+    wc, ws = O.quantize_operand(bf16_bits(T[:, torch.from_numpy(cols).cuda()].t().contiguous()), True)
+    assert np.array_equal(cc.view(N, M // 2)[torch.from_numpy(cols).cuda()].cpu().numpy(), wc)
+    assert np.array_equal(from_tiled(to_host_u8(sc), cols, M), ws)

@@ -55,3 +55,12 @@ def test_copy_probe(q):
     q.adahop_probe_copy(src, dst)
     torch.cuda.synchronize()
     assert torch.equal(src, dst)
+
+
+def test_fill_probe(q):
+    """src None: the write-only stream sets every bf16 of dst to 1.0 (bit pattern 0x3F80)."""
+    n = (32 << 20) + 24                       # 64 MiB of bf16 and a tail of three 16-byte words
+    dst = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    q.adahop_probe_copy(None, dst)
+    torch.cuda.synchronize()
+    assert bool((dst == 1.0).all())
