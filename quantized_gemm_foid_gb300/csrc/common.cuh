@@ -377,6 +377,12 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_
   return d;
 }
 
+// A shared-memory descriptor moved by off16 x 16 bytes: the start-address field is the low 14
+// bits, so while the address stays below 2^18 the addition never reaches the other fields.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
+  return d + off16;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major,
                                                        bool b_mn_major) {

@@ -425,6 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       constexpr uint32_t idesc_bf16 = make_idesc_bf16(C::kBM, BN, false, false);
+      // shared-memory descriptors of stage 0; a stage's are these plus its offset in the 16-byte
+      // address field
+      const uint64_t a0 = make_smem_desc(smem_base, 16, 1024, kLayoutSw128);
+      const uint64_t b0 = make_smem_desc(smem_base + C::kABytes, 16, 1024, kLayoutSw128);
+      const uint64_t sfa0 = make_smem_desc(smem_base + C::kSFA, 0, 128, kLayoutNone);
+      const uint64_t sfb0 = make_smem_desc(smem_base + C::kSFB, 0, 128, kLayoutNone);
       WorkIter it = make_iter(sched, pair);
       WorkItem w;
       while (ok && next_item<SK>(sched, it, w)) {
@@ -439,8 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sA = smem_base + stage * C::kStageBytes;
-          const uint32_t sB = sA + C::kABytes;
+          const uint32_t soff = (static_cast<uint32_t>(stage) * C::kStageBytes) >> 4;
           if (elect_one()) {
             if (step < num_k) {
               const uint32_t sfa_t = tmem + kSfTmemBase + stage * C::kSfCols;
@@ -455,14 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int kk = 0; kk < 4; ++kk) {
                 if (kk == 2 && half) break;
                 if ((kk & 1) == 0) {
-                  const int ka = kk >> 1;
-                  tmem_cp_32x128b_x4_pair(sfa_t + 4 * ka, make_smem_desc(sA + C::kSFA + 512 * ka, 0, 128, kLayoutNone));
-                  tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka, make_smem_desc(sA + C::kSFB + 512 * ka, 0, 128, kLayoutNone));
-                  tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka + 4,
-                                          make_smem_desc(sA + C::kSFB + 1024 + 512 * ka, 0, 128, kLayoutNone));
+                  const uint32_t ka = static_cast<uint32_t>(kk >> 1);
+                  tmem_cp_32x128b_x4_pair(sfa_t + 4 * ka, desc_add(sfa0, soff + 32 * ka));
+                  tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka, desc_add(sfb0, soff + 32 * ka));
+                  tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka + 4, desc_add(sfb0, soff + 64 + 32 * ka));
                 }
-                const uint64_t adesc = make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
-                const uint64_t bdesc = make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
+                const uint64_t adesc = desc_add(a0, soff + 2 * kk);
+                const uint64_t bdesc = desc_add(b0, soff + 2 * kk);
                 constexpr uint32_t idesc0 = make_idesc_mxf4(C::kBM, BN, 0, 0);
                 constexpr uint32_t idesc2 = make_idesc_mxf4(C::kBM, BN, 2, 2);
                 mma_mxf4_pair(tmem, adesc, bdesc, (kk & 1) ? idesc2 : idesc0, sfa_t + 4 * (kk >> 1),
@@ -472,11 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               // BF16 outlier tail: four K=16 MMAs over 128-byte rows (the first of a stream-K part
               // that starts with a tail stage overwrites the accumulator)
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t adesc = make_smem_desc(sA + 32 * kk, 16, 1024, kLayoutSw128);
-                const uint64_t bdesc = make_smem_desc(sB + 32 * kk, 16, 1024, kLayoutSw128);
-                mma_bf16_pair(tmem, adesc, bdesc, idesc_bf16, (step > w.kb || kk > 0) ? 1u : 0u);
-              }
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_pair(tmem, desc_add(a0, soff + 2 * kk), desc_add(b0, soff + 2 * kk), idesc_bf16,
+                              (step > w.kb || kk > 0) ? 1u : 0u);
             }
             tc_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);   // frees the stage in both CTAs
           }
