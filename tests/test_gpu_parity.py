@@ -255,10 +255,10 @@ def _rel(got, ref):
     return O.rel_frobenius(got, ref)
 
 
-# J <= 2048 and J > 2048 run different pipeline configurations of the kernel (2304: an odd
-# multiple of 128, whose last slice is half full)
+# J <= 2048 and J > 2048 run different pipeline configurations of the kernel (384, 2176 and 2432:
+# odd multiples of 128, whose last 256-wide slice of J is half full)
 @pytest.mark.parametrize("P,Q,J", [(128, 256, 256), (256, 512, 384), (384, 384, 1024), (128, 128, 128),
-                                   (256, 384, 2304), (384, 256, 4096)])
+                                   (128, 256, 2176), (256, 384, 2304), (256, 128, 2432), (384, 256, 4096)])
 @pytest.mark.parametrize("r", [0, 16, 64, 128])
 @pytest.mark.parametrize("out", ["fp32", "bf16"])
 @pytest.mark.parametrize("stream_k", [False, True])
