@@ -418,6 +418,50 @@ class Bench:
                        "shape": [c.M, c.N]}
         return out
 
+    def other_kernels(self, peaks: dict, reps: int = 10) -> dict:
+        """The step's other kernels against their own rooflines, each timed alone (launches queued
+        ahead of the device): K6, the BF16 GEMM of the BF16 strategy and baseline, on the q
+        projection's Fwd (32768 x 4096 x 4096) against the burst BF16 peak; K1, FOID's row
+        probe of the gate projection's G_Y (r = 64); K5 + K4, the gate dgrad's outer-OE outlier
+        GEMM with the scatter-add fused, a 256 MB write before each launch so that W comes from
+        DRAM.  FOID and the outlier GEMM against the measured copy rate."""
+        q = self.q
+        hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        bf16_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        out = {}
+        c = self.cases[0]                                       # q: N = K = 4096
+        ms = cuda_time_ms(lambda: q.adahop_gemm_bf16(c.X, 1, c.W, 1, c.M, c.N, c.K, c.Y, self.ws), 3, hold=True)
+        tf = 2 * c.M * c.N * c.K / ms / 1e9
+        out["k6_bf16_gemm"] = {"shape": [c.M, c.N, c.K], "ms": round(ms, 4), "tflops": round(tf, 1),
+                               "frac": round(tf / bf16_peak, 3), "peak": bf16_peak, "bound": "tensor"}
+        g = max(self.cases, key=lambda c: c.M * c.N)            # gate: N = 14336
+        r = 64
+        idx = torch.empty(r, dtype=torch.int32, device=self.device)
+        mask = torch.empty((g.M + 31) // 32, dtype=torch.int32, device=self.device)
+        fws = q.new_workspace(q.adahop_foid_workspace_size(g.M, r), device=self.device)
+        ms = cuda_time_ms(lambda: q.adahop_foid(g.GY, 0, r, idx, mask, fws), reps, hold=True)
+        nbytes = 64 * g.M * 2 + 4 * r + g.M // 8
+        out["k1_foid"] = {"lines": g.M, "r": r, "us": round(ms * 1e3, 2), "gbs": round(nbytes / ms / 1e6, 1),
+                          "frac": round(nbytes / ms / 1e6 / hbm, 3), "bound": "latency"}
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=self.device)
+        A = g.GY[:r]                                            # r rows of G_Y: r x N
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        hold_device(reps, 200.0)
+        for s0, s1 in ev:
+            flush.fill_(1)
+            s0.record()
+            q.adahop_gemm_bf16_scatter_add(A, 1, g.W, 0, r, g.K, g.N, g.dX, idx, r, 0, self.ws)
+            s1.record()
+        torch.cuda.synchronize()
+        us = 1e3 * sum(a.elapsed_time(b) for a, b in ev) / reps
+        nbytes = 2 * (g.N * g.K + r * g.N + 2 * r * g.K)
+        out["k5_k4_outlier_gemm_scatter"] = {"shape": [r, g.K, g.N], "us": round(us, 2),
+                                             "gbs": round(nbytes / us / 1e3, 1),
+                                             "frac": round(nbytes / us / 1e3 / hbm, 3), "bound": "hbm"}
+        del flush
+        return out
+
     # ------------------------------------------------------------------ end to end (host buffers)
     def e2e(self, steps: int, warmup: int, trials: int = 1):
         """Same metric through the C ABI with pinned host buffers: every step copies X, W, G_Y of
@@ -1298,6 +1342,7 @@ def main():
     copy_gbs = copy_probe(q, device)
     fill_gbs = fill_probe(q, device)
     prep = b.prep_bandwidth()
+    others = b.other_kernels(peaks)
     variants = b.variants()
     clocks = sampler.stop()
     st = q.adahop_get_device_status(b.ws)
@@ -1328,6 +1373,7 @@ def main():
                  "copy_probe_gbs": copy_gbs, "fill_probe_gbs": fill_gbs, "nominal_gbs": NOMINAL["hbm_gbs"],
                  **{k: dict(v, frac=round(v["gbs"] / hbm, 3), frac_copy_probe=round(v["gbs"] / copy_gbs, 3),
                             frac_nominal=round(v["gbs"] / NOMINAL["hbm_gbs"], 3)) for k, v in prep.items()}},
+        "other_kernels": others,
         "variants": variants,
         "execution": "the step captured once in a CUDA graph and replayed (every launch of the step "
                      "runs on every replay)",
