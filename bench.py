@@ -1006,7 +1006,9 @@ def batch_sweep(q, device, args):
     """Throughput against batch size (the pages' Fig. 6 analogue): the Llama3.1-8B block's seven
     linears, Fwd + dgrad + wgrad, at M = seq_len x batch tokens per step for seq_len 4096 and
     batch 1..16, under the calibrated AdaHOP plan and under the all-BF16 plan on the same kernels.
-    CUDA events over 5 steps after 3 warm-up steps.  Prints one JSON object."""
+    CUDA events over 5 steps after 3 warm-up steps, the step replayed as a CUDA graph (the
+    call-by-call time beside it; the two alternated three times, medians).  Prints one JSON
+    object."""
     import dataclasses
     base = WORKLOADS[WORKLOAD]
     points = []
@@ -1020,11 +1022,21 @@ def batch_sweep(q, device, args):
                 c.plan.fwd, c.plan.dgrad, c.plan.wgrad = orig if strat is None else (strat, strat, strat)
             for _ in range(3):
                 b.step()
+            graph = b.capture()                 # the step as the bench line times it
+            for _ in range(3):
+                graph.replay()
             torch.cuda.synchronize()
-            ms = cuda_time_ms(b.step, 5)
+            # graph and call-by-call alternated three times (the power-capped clock drifts between
+            # consecutive short windows), medians reported
+            g_ms, e_ms = [], []
+            for _ in range(3):
+                g_ms.append(cuda_time_ms(graph.replay, 5))
+                e_ms.append(cuda_time_ms(b.step, 5))
+            ms, eager = statistics.median(g_ms), statistics.median(e_ms)
+            del graph
             assert q.adahop_get_device_status(b.ws) == 0
             row[name] = {"ms_per_step": round(ms, 3), "tokens_per_s": round(M / ms * 1e3),
-                         "eff_tflops": round(b.flops_per_step / ms / 1e9, 1)}
+                         "eff_tflops": round(b.flops_per_step / ms / 1e9, 1), "eager_ms_per_step": round(eager, 3)}
         row["speedup_vs_bf16"] = round(row["bf16"]["ms_per_step"] / row["adahop"]["ms_per_step"], 3)
         points.append(row)
         del b
@@ -1332,7 +1344,14 @@ def main():
     ms = cuda_time_ms(graph.replay, args.steps)
     barrier(world)
     ms = max_over_ranks(world, ms)
-    eager_ms = max_over_ranks(world, cuda_time_ms(b.step, args.steps))
+    # the same step launched call by call, alternated with graph replays (the power-capped clock
+    # drifts between consecutive windows): medians of three windows each, for comparison only
+    g_cmp, e_cmp = [], []
+    for _ in range(3):
+        e_cmp.append(cuda_time_ms(b.step, args.steps))
+        g_cmp.append(cuda_time_ms(graph.replay, args.steps))
+    eager_ms = max_over_ranks(world, statistics.median(e_cmp))
+    graph_cmp_ms = max_over_ranks(world, statistics.median(g_cmp))
     del graph
     gemm_clocks = ClockSampler(gpu_index)
     gemm_clocks.start()
@@ -1380,7 +1399,9 @@ def main():
         "execution": "the step captured once in a CUDA graph and replayed (every launch of the step "
                      "runs on every replay)",
         "eager": {"ms_per_step": eager_ms, "value": whole_job_tflops(b.flops_per_step, world, eager_ms),
-                  "note": "the same step launched call by call through the C ABI"},
+                  "graph_ms_per_step_alternated": graph_cmp_ms,
+                  "note": "the same step launched call by call through the C ABI; median of three windows "
+                          "alternated with three graph-replay windows (graph_ms_per_step_alternated)"},
         "gemms": per_gemm,
         "clocks": clocks,
         "e2e": {"value": whole_job_tflops(b.flops_per_step, world, e2e_ms), "unit": "TFLOP/s",
