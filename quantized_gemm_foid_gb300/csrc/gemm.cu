@@ -434,12 +434,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       WorkIter it = make_iter(sched, pair);
       WorkItem w;
       while (ok && next_item<SK>(sched, it, w)) {
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.acc_empty), acc_phase ^ 1u, abort_flag))) {
-          ok = false;
-          break;
+        // The item's first stage, peeled from the loop: its scale copies go to their own
+        // tensor-memory columns while the epilogue still drains the accumulator, and only its
+        // MMAs wait for the drain.
+        {
+          const int step = w.kb;
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t soff = (static_cast<uint32_t>(stage) * C::kStageBytes) >> 4;
+          const uint32_t sfa_t = tmem + kSfTmemBase + stage * C::kSfCols;
+          const uint32_t sfb_t = sfa_t + 8;
+          const bool half = (step == num_k - 1) && ((g.J & 255) != 0);
+          if (step < num_k && elect_one()) {
+#pragma unroll
+            for (uint32_t ka = 0; ka < 2; ++ka) {
+              if (ka == 1 && half) break;
+              tmem_cp_32x128b_x4_pair(sfa_t + 4 * ka, desc_add(sfa0, soff + 32 * ka));
+              tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka, desc_add(sfb0, soff + 32 * ka));
+              tmem_cp_32x128b_x4_pair(sfb_t + 8 * ka + 4, desc_add(sfb0, soff + 64 + 32 * ka));
+            }
+          }
+          __syncwarp();
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.acc_empty), acc_phase ^ 1u, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            if (step < num_k) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                if (kk == 2 && half) break;
+                constexpr uint32_t idesc0 = make_idesc_mxf4(C::kBM, BN, 0, 0);
+                constexpr uint32_t idesc2 = make_idesc_mxf4(C::kBM, BN, 2, 2);
+                mma_mxf4_pair(tmem, desc_add(a0, soff + 2 * kk), desc_add(b0, soff + 2 * kk),
+                              (kk & 1) ? idesc2 : idesc0, sfa_t + 4 * (kk >> 1), sfb_t + 8 * (kk >> 1),
+                              kk > 0 ? 1u : 0u);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_pair(tmem, desc_add(a0, soff + 2 * kk), desc_add(b0, soff + 2 * kk), idesc_bf16,
+                              kk > 0 ? 1u : 0u);
+            }
+            tc_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);
+          }
+          __syncwarp();
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        tc_fence_after();
-        for (int step = w.kb; step < w.ke; ++step) {
+        for (int step = w.kb + 1; step < w.ke; ++step) {
           if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag))) {
             ok = false;
             break;
