@@ -98,6 +98,43 @@ def _read_blocks(path):
     return blocks
 
 
+def test_quantize_operand_worked_by_hand():
+    """The whole operand path (outlier lines zeroed, block-32 Hadamard along J, E8M0 + E2M1,
+    nibble packing) on a 2 x 64 operand worked out from closed forms, with no oracle helper:
+    row 0 = [1.0] * 32 (a constant block) followed by one 2.0 at position 5 of the second block;
+    row 1 = anything, but it is an extracted outlier line (zeroed).
+
+    Block 0: the Hadamard of a constant is (32 c, 0, ..., 0) with c = RN32(1/sqrt 32), so the
+    block amax is 5.6568... -> E8M0 byte floor(log2 5.66) - 2 + 127 = 127, scale 1, and 5.66
+    rounds to the E2M1 value 6 (code 7); every other element is +0 (code 0).
+    Block 1: H e_5 has entries (-1)^popcount(i & 5) (Sylvester), times 2c = 0.3536: amax 0.3536
+    -> byte floor(log2 0.354) - 2 + 127 = 123, scale 2^-4, |v| = 5.66 -> code 7, sign bit 8 where
+    popcount(i & 5) is odd.  Row 1: codes 0, scale byte 0 (an all-zero block)."""
+    one = np.uint16(0x3F80)                 # bf16 1.0
+    two = np.uint16(0x4000)                 # bf16 2.0
+    T = np.zeros((2, 64), dtype=np.uint16)
+    T[0, :32] = one
+    T[0, 32 + 5] = two
+    T[1, :] = one                           # nonzero, but zeroed as an extracted line
+    packed, scales = O.quantize_operand(T, True, zero_rows=[1])
+    want_codes = np.zeros((2, 64), dtype=np.uint8)
+    want_codes[0, 0] = 7
+    for i in range(32):
+        want_codes[0, 32 + i] = 7 | (8 if bin(i & 5).count("1") % 2 else 0)
+    want_packed = (want_codes[:, 0::2] | (want_codes[:, 1::2] << 4)).astype(np.uint8)
+    assert np.array_equal(scales, np.array([[127, 123], [0, 0]], dtype=np.uint8))
+    assert np.array_equal(packed, want_packed)
+    # without the transform the same row quantises its raw values: block 0 all 1.0 (byte
+    # floor(log2 1) - 2 + 127 = 125, scale 2^-2, v = 4 -> code 6); block 1 one 2.0 (byte 126,
+    # v = 4 -> code 6 at position 5, zeros elsewhere)
+    packed, scales = O.quantize_operand(T[:1], False)
+    want = np.zeros(64, dtype=np.uint8)
+    want[:32] = 6
+    want[32 + 5] = 6
+    assert np.array_equal(scales[0], np.array([125, 126], dtype=np.uint8))
+    assert np.array_equal(packed[0], (want[0::2] | (want[1::2] << 4)).astype(np.uint8))
+
+
 def test_mxfp4_hand_worked_blocks(golden_dir):
     for b in _read_blocks(os.path.join(golden_dir, "mxfp4_worked_blocks.txt")):
         z = np.array(b["vals"], dtype=np.float32)
