@@ -335,6 +335,11 @@ def test_calibration_recovers_configured_patterns():
     assert max(rr, rc) < 2.0
     rr, rc = O.calibration_ratios(bf16_bits(X))
     assert rc > 100 * O.DEFAULT_TAU
+    # the whole calibration: the pattern pairs (X, W) = CN, (G_Y, W) = RN, (G_Y, X) = RC take
+    # IHT, OE-Left and OE-Left (the pages' strategy table)
+    plan = O.calibrate(bf16_bits(X), bf16_bits(W), bf16_bits(GY))
+    assert plan["patterns"] == {"X": O.PAT_COL, "W": O.PAT_NONE, "GY": O.PAT_ROW}
+    assert (plan["fwd"], plan["dgrad"], plan["wgrad"]) == (O.IHT, O.OE_LEFT, O.OE_LEFT)
 
 
 def test_strategy_map():
