@@ -180,9 +180,10 @@ def test_instella_3b_config_sampled(q, li):
     _sampled_parity(q, "instella-3b", li, dtype=torch.bfloat16)
 
 
-@pytest.mark.parametrize("li", [1, 4, 6])
+@pytest.mark.parametrize("li", [1, 3, 4, 6])
 def test_llama_8b_config_sampled(q, li):
     """Full-size Llama3.1-8B linears in the bench's launch configuration, checked on sampled rows
-    of all three GEMMs: k (N = 1024: the J = 1024 dgrad), gate (N = 14336, K = 4096) and down
-    (N = 4096, K = 14336: J = 14336 in Fwd, Q = 14336 in dgrad)."""
+    of all three GEMMs: k (N = 1024: the J = 1024 dgrad), o (N = K = 4096: its wgrad, 4096 x 4096
+    x 32768 with the rank-64 tail, runs stream-K), gate (N = 14336, K = 4096) and down (N = 4096,
+    K = 14336: J = 14336 in Fwd, Q = 14336 in dgrad)."""
     _sampled_parity(q, "llama3.1-8b", li, n_rows=32, n_cols=96, dtype=torch.bfloat16)
