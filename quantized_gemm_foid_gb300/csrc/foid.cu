@@ -318,11 +318,13 @@ __device__ void foid_merge_cta(uint64_t *sk_flat, const uint64_t *cand, int runs
   uint64_t top[KPL];
 #pragma unroll
   for (int s = 0; s < KPL; ++s) top[s] = 0ull;
-  // four runs' loads in flight per warp, then their merges
-  for (int run0 = warp; run0 < runs; run0 += 4 * nwarps) {
-    uint64_t b[4][KPL];
+  // kFly runs' loads in flight per warp, then their merges: one round of L2 reads covers all 128
+  // runs of a 32768-line probe (eight keys per lane at r = 256 would spill, so four there)
+  constexpr int kFly = KPL >= 8 ? 4 : 8;
+  for (int run0 = warp; run0 < runs; run0 += kFly * nwarps) {
+    uint64_t b[kFly][KPL];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kFly; ++u) {
       const int run = run0 + u * nwarps;
 #pragma unroll
       for (int s = 0; s < KPL; ++s) {
@@ -331,7 +333,7 @@ __device__ void foid_merge_cta(uint64_t *sk_flat, const uint64_t *cand, int runs
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) run_merge<KPL>(top, b[u], lane);
+    for (int u = 0; u < kFly; ++u) run_merge<KPL>(top, b[u], lane);
   }
 #pragma unroll
   for (int s = 0; s < KPL; ++s) sk[warp][32 * s + lane] = top[s];
